@@ -1,0 +1,257 @@
+"""GB300-native tensor-parallel row-parallel linear epilogue.
+
+Thin Python binding of ``libare.so`` (C ABI in ``include/are.h``): argument
+marshalling only.  Every step of the computation runs in the library's CUDA
+kernels; PyTorch supplies device memory and streams.  There is no CPU path:
+calling any operation without the built library raises ``AreLibraryMissing``.
+
+Operations (the same names as the C ABI, without the ``are_`` prefix):
+
+* ``gemm_rs(A, B, out, ws)``      R partial GEMMs, ring-order fp32 sum,
+  reduce-scattered into R owner row segments (bf16).
+* ``gemm_ar(A, B, out, ws)``      R partial GEMMs rounded to bf16, all-reduced
+  into every rank view.
+* ``allreduce_rmsnorm(partials, residual, gamma, eps, out, ws)``
+  all-reduce + residual + RMSNorm in one Lamport-synchronised kernel.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libare.so")
+
+# status codes (are_status)
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBUSY, ENODEV, ECAPACITY = range(8)
+# ops
+OP_GEMM_RS, OP_GEMM_AR, OP_ALLREDUCE_RMSNORM = 1, 2, 3
+# debug flags
+DEBUG_NO_REARM, DEBUG_LOG_PIECES, DEBUG_COUNT_CANON, DEBUG_SKIP_PUBLISH, DEBUG_SKIP_STAGE = 1, 2, 4, 8, 16
+# device status codes
+DEV_OK, DEV_MASK_TIMEOUT, DEV_STAGE_TIMEOUT, DEV_PIPE_TIMEOUT = 0, 1, 2, 3
+# snapshot kinds
+SNAP_MASKS, SNAP_STAGING, SNAP_PIECES, SNAP_COUNTERS = 1, 2, 3, 4
+PIECE_WORDS = 64
+TILE_M, TILE_N = 128, 256
+
+# Every C-ABI symbol declared in include/are.h.
+EXPORTS = [
+    "are_version", "are_status_string", "are_supports", "are_workspace_create", "are_workspace_destroy",
+    "are_workspace_reset", "are_workspace_set_debug", "are_get_device_status", "are_debug_snapshot",
+    "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm",
+]
+
+
+class AreError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+class AreLibraryMissing(RuntimeError):
+    pass
+
+
+class _Caps(ctypes.Structure):
+    _fields_ = [("R_max", ctypes.c_int32), ("M_max", ctypes.c_int64), ("N_max", ctypes.c_int64),
+                ("K_max", ctypes.c_int64), ("timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_uint32),
+                ("reserved", ctypes.c_uint32)]
+
+
+class _DevStatus(ctypes.Structure):
+    _fields_ = [("code", ctypes.c_uint32), ("where", ctypes.c_uint32), ("a", ctypes.c_int32), ("b", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load ``libare.so`` (idempotent).  Raises AreLibraryMissing if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise AreLibraryMissing(
+            f"{path} is not built; run `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, u32, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
+    lib.are_version.restype = i32
+    lib.are_status_string.restype = ctypes.c_char_p
+    lib.are_status_string.argtypes = [i32]
+    lib.are_supports.restype = i32
+    lib.are_supports.argtypes = [i32, i32, i64, i64, i64]
+    lib.are_workspace_create.restype = i32
+    lib.are_workspace_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(_Caps)]
+    lib.are_workspace_destroy.restype = i32
+    lib.are_workspace_destroy.argtypes = [vp]
+    lib.are_workspace_reset.restype = i32
+    lib.are_workspace_reset.argtypes = [vp]
+    lib.are_workspace_set_debug.restype = i32
+    lib.are_workspace_set_debug.argtypes = [vp, u32, i64]
+    lib.are_get_device_status.restype = i32
+    lib.are_get_device_status.argtypes = [vp, ctypes.POINTER(_DevStatus)]
+    lib.are_debug_snapshot.restype = i32
+    lib.are_debug_snapshot.argtypes = [vp, i32, vp, ctypes.c_size_t]
+    for name in ("are_gemm_rs", "are_gemm_ar"):
+        f = getattr(lib, name)
+        f.restype = i32
+        f.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp]
+    lib.are_allreduce_rmsnorm.restype = i32
+    lib.are_allreduce_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i64, i64, vp, vp]
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().are_status_string(status).decode()
+    except AreLibraryMissing:
+        return f"status {status}"
+
+
+def version() -> int:
+    return load_library().are_version()
+
+
+def supports(op: int, R: int, M: int, N: int, K: int = 0) -> bool:
+    return load_library().are_supports(op, R, M, N, K) == OK
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise AreError(status, what)
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _ptrs(tensors) -> ctypes.Array:
+    return (ctypes.c_void_p * len(tensors))(*[t.data_ptr() for t in tensors])
+
+
+def _check_bf16(t, what: str):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA bfloat16 tensor")
+
+
+class Workspace:
+    """Device workspace (tile masks, partial buffer, armed staging, status word).
+
+    Sized once from the capacities; use one workspace per stream."""
+
+    def __init__(self, R_max: int, M_max: int, N_max: int, K_max: int = 0, timeout_ns: int = 0,
+                 debug_flags: int = 0):
+        lib = load_library()
+        caps = _Caps(R_max, M_max, N_max, K_max, timeout_ns, debug_flags, 0)
+        h = ctypes.c_void_p()
+        _check(lib.are_workspace_create(ctypes.byref(h), ctypes.byref(caps)), "are_workspace_create")
+        self._h = h
+        self.caps = dict(R_max=R_max, M_max=M_max, N_max=N_max, K_max=K_max)
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("workspace is closed")
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load_library().are_workspace_destroy(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self):
+        _check(load_library().are_workspace_reset(self.handle), "are_workspace_reset")
+
+    def set_debug(self, flags: int, arg: int = -1):
+        _check(load_library().are_workspace_set_debug(self.handle, flags, arg), "are_workspace_set_debug")
+
+    def device_status(self) -> dict:
+        st = _DevStatus()
+        rc = load_library().are_get_device_status(self.handle, ctypes.byref(st))
+        if rc not in (OK, ETIMEOUT):
+            raise AreError(rc, "are_get_device_status")
+        return {"status": rc, "code": st.code, "where": st.where, "a": st.a, "b": st.b}
+
+    def snapshot(self, kind: int, nbytes: int):
+        import numpy as np
+        buf = np.empty(nbytes, dtype=np.uint8)
+        _check(load_library().are_debug_snapshot(self.handle, kind, buf.ctypes.data, nbytes), "are_debug_snapshot")
+        return buf
+
+
+def gemm_rs(A: Sequence, B: Sequence, out, ws: Workspace, stream=None):
+    """out[s] = rows [s*M/R, (s+1)*M/R) of bf16(sum_r A[r] @ B[r]).
+
+    ``out`` is either a list of R segment tensors [M/R, N] or one [M, N]
+    tensor (segments are then its consecutive row bands)."""
+    R = len(A)
+    M, K = A[0].shape
+    N = B[0].shape[1]
+    for t in list(A) + list(B):
+        _check_bf16(t, "A/B")
+    if isinstance(out, (list, tuple)):
+        segs = list(out)
+        for t in segs:
+            _check_bf16(t, "out")
+        seg_ptrs = (ctypes.c_void_p * R)(*[t.data_ptr() for t in segs])
+    else:
+        _check_bf16(out, "out")
+        S = M // R if R else 0
+        seg_ptrs = (ctypes.c_void_p * R)(*[out.data_ptr() + s * S * N * 2 for s in range(R)])
+    rc = load_library().are_gemm_rs(_ptrs(A), _ptrs(B), seg_ptrs, R, M, N, K, ws.handle, _stream_handle(stream))
+    _check(rc, "are_gemm_rs")
+
+
+def gemm_ar(A: Sequence, B: Sequence, out, ws: Workspace, stream=None):
+    """Every view out[v] = bf16(sum_r f32(bf16(A[r] @ B[r]))).
+
+    ``out`` is a list of R [M, N] views (they may alias) or one tensor used
+    for every view."""
+    R = len(A)
+    M, K = A[0].shape
+    N = B[0].shape[1]
+    for t in list(A) + list(B):
+        _check_bf16(t, "A/B")
+    views = list(out) if isinstance(out, (list, tuple)) else [out] * R
+    for t in views:
+        _check_bf16(t, "out")
+    rc = load_library().are_gemm_ar(_ptrs(A), _ptrs(B), _ptrs(views), R, M, N, K, ws.handle, _stream_handle(stream))
+    _check(rc, "are_gemm_ar")
+
+
+def allreduce_rmsnorm(partials: Sequence, residual, gamma, eps: float, out, ws: Workspace, stream=None):
+    """out = bf16(rmsnorm(sum_r partials[r] + residual) * gamma)."""
+    import torch
+    R = len(partials)
+    M, N = partials[0].shape
+    for t in partials:
+        _check_bf16(t, "partials")
+    if residual is not None:
+        _check_bf16(residual, "residual")
+    _check_bf16(out, "out")
+    if gamma.dtype != torch.float32 or not gamma.is_cuda or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous CUDA float32 tensor")
+    rc = load_library().are_allreduce_rmsnorm(
+        _ptrs(partials), residual.data_ptr() if residual is not None else None, gamma.data_ptr(), float(eps),
+        out.data_ptr(), R, M, N, ws.handle, _stream_handle(stream))
+    _check(rc, "are_allreduce_rmsnorm")

@@ -1,0 +1,410 @@
+// C ABI of the library: argument validation, workspace lifecycle, launches.
+//
+// Lessons from the pages that shape this layer:
+//  * ROCm/mori PR #662 (review threads): one predicate shared by the
+//    "supports" query and the execution path; validation before any
+//    allocation or launch; a failed setup releases what it acquired and
+//    returns the original error; buffer offsets sized by capacity so the
+//    layout never moves with M.
+//  * ROCm/aiter PR #4977 (bring-up and follow-up commits): the Lamport staging
+//    region is private to this kernel, armed once outside any graph capture
+//    (on a private stream), and the persistent grid is clamped to the
+//    co-resident block count.
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "are_internal.h"
+
+using namespace are;
+
+struct are_ws {
+    int device = 0;
+    int num_sms = 0;
+    are_caps caps{};
+    DevStatus* d_status = nullptr;
+    unsigned long long* d_counters = nullptr;
+    uint32_t* d_mask = nullptr;
+    size_t mask_words = 0;
+    uint8_t* d_part = nullptr;
+    size_t part_bytes = 0;
+    int32_t* d_pieces = nullptr;
+    size_t piece_words = 0;
+    uint32_t* d_staging = nullptr;
+    size_t staging_words = 0;
+    int ar_resident[17] = {0};
+    std::mutex mu;
+    uint32_t debug_flags = 0;
+    int64_t debug_arg = -1;
+    uint64_t timeout_ns = 0;
+    int64_t last_ar_M = 0, last_ar_N = 0;
+};
+
+namespace {
+
+constexpr uint64_t kDefaultTimeoutNs = 200ull * 1000 * 1000;
+constexpr size_t kCounterWords = 4;
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+are_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return ARE_OK;
+    if (e == cudaErrorMemoryAllocation) return ARE_ENOMEM;
+    return ARE_ECUDA;
+}
+
+struct TryLock {
+    std::mutex& m;
+    bool ok;
+    explicit TryLock(std::mutex& mm) : m(mm), ok(mm.try_lock()) {}
+    ~TryLock() {
+        if (ok) m.unlock();
+    }
+};
+
+void free_ws(are_ws* ws) {
+    if (!ws) return;
+    cudaFree(ws->d_status);
+    cudaFree(ws->d_counters);
+    cudaFree(ws->d_mask);
+    cudaFree(ws->d_part);
+    cudaFree(ws->d_pieces);
+    cudaFree(ws->d_staging);
+    delete ws;
+}
+
+// Zero the bookkeeping and arm the staging buffer on a private non-blocking
+// stream, then wait for it.  Never on the caller's stream (a captured arming
+// would re-arm on every replay).
+are_status arm_workspace(are_ws* ws) {
+    cudaStream_t s = nullptr;
+    cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws->d_status, 0, sizeof(DevStatus), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws->d_counters, 0, kCounterWords * 8, s);
+    if (e == cudaSuccess && ws->d_mask) e = cudaMemsetAsync(ws->d_mask, 0, ws->mask_words * 4, s);
+    if (e == cudaSuccess && ws->d_pieces) e = cudaMemsetAsync(ws->d_pieces, 0, ws->piece_words * 4, s);
+    if (e == cudaSuccess && ws->d_staging) e = launch_fill_u32(ws->d_staging, kSentinelF32, ws->staging_words, s);
+    cudaError_t e2 = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = e2;
+    cudaStreamDestroy(s);
+    return from_cuda(e);
+}
+
+bool ranks_ok(int R) { return R >= 1 && R <= kMaxRanks; }
+
+// A device pointer must be 16-byte aligned; it may be NULL only when the
+// tensor it stands for has no elements.
+bool ptr_ok(const void* p, int64_t elems) { return elems == 0 ? (p == nullptr || aligned16(p)) : aligned16(p); }
+
+are_status check_gemm_ptrs(const are_bf16* const A[], const are_bf16* const B[], are_bf16* const out[], int R,
+                           int64_t M, int64_t N, int64_t K, int mode) {
+    if (!A || !B || !out) return ARE_EINVAL;
+    const int64_t out_elems = (mode == kModeRS) ? (M / R) * N : M * N;
+    for (int r = 0; r < R; ++r)
+        if (!ptr_ok(A[r], M * K) || !ptr_ok(B[r], K * N) || !ptr_ok(out[r], out_elems)) return ARE_EINVAL;
+    return ARE_OK;
+}
+
+are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const B[], are_bf16* const out[], int R,
+                     int64_t M, int64_t N, int64_t K, are_ws* ws, void* stream) {
+    if (!ws) return ARE_EINVAL;
+    const int op = (mode == kModeRS) ? ARE_OP_GEMM_RS : ARE_OP_GEMM_AR;
+    are_status st = are_supports(op, R, M, N, K);
+    if (st != ARE_OK) return st;
+    st = check_gemm_ptrs(A, B, out, R, M, N, K, mode);
+    if (st != ARE_OK) return st;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    if (R > ws->caps.R_max || M > ws->caps.M_max || N > ws->caps.N_max || K > ws->caps.K_max || !ws->d_part)
+        return ARE_ECAPACITY;
+    const int64_t tiles_m = ceil_div(M, kBM), tiles_n = ceil_div(N, kBN);
+    const int64_t T = tiles_m * tiles_n;
+    if ((size_t)T > ws->mask_words || (size_t)(R * T) * kTilePartBytes > ws->part_bytes) return ARE_ECAPACITY;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (M == 0 || N == 0) return ARE_OK;
+
+    // distinct output views (GEMM+AR views may alias)
+    int nviews = 0;
+    const are_bf16* views[kMaxRanks];
+    if (mode == kModeAR) {
+        for (int v = 0; v < R; ++v) {
+            bool dup = false;
+            for (int w = 0; w < nviews; ++w) dup |= (views[w] == out[v]);
+            if (!dup) views[nviews++] = out[v];
+        }
+    }
+    if (K == 0) {  // empty contraction: the result is zero
+        if (mode == kModeRS) {
+            for (int r = 0; r < R; ++r) {
+                cudaError_t e = cudaMemsetAsync(out[r], 0, (size_t)(M / R) * N * 2, s);
+                if (e != cudaSuccess) return from_cuda(e);
+            }
+        } else {
+            for (int v = 0; v < nviews; ++v) {
+                cudaError_t e = cudaMemsetAsync(const_cast<are_bf16*>(views[v]), 0, (size_t)M * N * 2, s);
+                if (e != cudaSuccess) return from_cuda(e);
+            }
+        }
+        return ARE_OK;
+    }
+
+    GemmParams* p = new (std::nothrow) GemmParams;
+    if (!p) return ARE_ENOMEM;
+    std::memset(p, 0, sizeof(GemmParams));
+    cudaError_t e = cudaSuccess;
+    const int64_t S = (mode == kModeRS) ? M / R : M;
+    int H = 128;
+    if (mode == kModeRS) {
+        while (S % H) H >>= 1;  // largest power of two dividing S, <= 128 (>= 8 by are_supports)
+    }
+    for (int r = 0; r < R && e == cudaSuccess; ++r) {
+        e = make_tmap_bf16(&p->tmA[r], A[r], (uint64_t)K, (uint64_t)M, kBK, kBM);
+        if (e == cudaSuccess) e = make_tmap_bf16(&p->tmB[r], B[r], (uint64_t)N, (uint64_t)K, 64, kBK);
+        if (e == cudaSuccess && mode == kModeRS)
+            e = make_tmap_bf16(&p->tmOut[r], out[r], (uint64_t)N, (uint64_t)S, 64, (uint32_t)H);
+    }
+    for (int v = 0; v < nviews && e == cudaSuccess; ++v)
+        e = make_tmap_bf16(&p->tmOut[v], views[v], (uint64_t)N, (uint64_t)M, 64, kBM);
+    if (e != cudaSuccess) {
+        delete p;
+        return ARE_EINVAL;
+    }
+    p->part = ws->d_part;
+    p->mask = ws->d_mask;
+    p->status = ws->d_status;
+    p->pieces = ws->d_pieces;
+    p->R = R;
+    p->M = (int)M;
+    p->N = (int)N;
+    p->K = (int)K;
+    p->S = (int)S;
+    p->H = H;
+    p->nviews = nviews;
+    p->tiles_m = (int)tiles_m;
+    p->tiles_n = (int)tiles_n;
+    p->num_tiles = (int)T;
+    p->num_units = (int)(T * R);
+    p->num_kb = (int)ceil_div(K, kBK);
+    p->group_m = (int)std::min<int64_t>(tiles_m, 8);
+    p->flags = ws->debug_flags;
+    p->debug_arg = ws->debug_arg;
+    p->timeout_ns = ws->timeout_ns;
+    const int grid = (int)std::min<int64_t>(p->num_units, ws->num_sms);
+    e = launch_gemm_reduce(*p, mode, grid, s);
+    delete p;
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int are_version(void) { return (1 << 16) | 0; }
+
+const char* are_status_string(are_status s) {
+    switch (s) {
+        case ARE_OK: return "ARE_OK";
+        case ARE_EINVAL: return "ARE_EINVAL: invalid argument";
+        case ARE_ENOMEM: return "ARE_ENOMEM: device allocation failed";
+        case ARE_ECUDA: return "ARE_ECUDA: CUDA call or launch failed";
+        case ARE_ETIMEOUT: return "ARE_ETIMEOUT: a bounded device wait expired";
+        case ARE_EBUSY: return "ARE_EBUSY: workspace in use by another thread";
+        case ARE_ENODEV: return "ARE_ENODEV: current device is not sm_103";
+        case ARE_ECAPACITY: return "ARE_ECAPACITY: call exceeds workspace capacity";
+    }
+    return "unknown are_status";
+}
+
+are_status are_supports(int op, int R, int64_t M, int64_t N, int64_t K) {
+    const int64_t kLim = (int64_t)1 << 31;
+    if (!ranks_ok(R) || M < 0 || N < 0 || M >= kLim || N >= kLim) return ARE_EINVAL;
+    switch (op) {
+        case ARE_OP_GEMM_RS:
+            if (K < 0 || K >= kLim || K % 8 || N % 8 || M % R || (M / R) % 8) return ARE_EINVAL;
+            if (ceil_div(M, kBM) * ceil_div(N, kBN) * R >= kLim) return ARE_EINVAL;
+            return ARE_OK;
+        case ARE_OP_GEMM_AR:
+            if (K < 0 || K >= kLim || K % 8 || N % 8) return ARE_EINVAL;
+            if (ceil_div(M, kBM) * ceil_div(N, kBN) * R >= kLim) return ARE_EINVAL;
+            return ARE_OK;
+        case ARE_OP_ALLREDUCE_RMSNORM:
+            if (N % 8 || N > 32768) return ARE_EINVAL;
+            return ARE_OK;
+        default:
+            return ARE_EINVAL;
+    }
+}
+
+are_status are_workspace_create(are_ws** out, const are_caps* caps) {
+    if (!out || !caps) return ARE_EINVAL;
+    *out = nullptr;
+    if (!ranks_ok(caps->R_max) || caps->M_max < 1 || caps->N_max < 8 || caps->N_max % 8 || caps->K_max < 0)
+        return ARE_EINVAL;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return ARE_ENODEV;
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (prop.major != 10 || prop.minor != 3) return ARE_ENODEV;
+
+    are_ws* ws = new (std::nothrow) are_ws;
+    if (!ws) return ARE_ENOMEM;
+    ws->device = dev;
+    ws->num_sms = prop.multiProcessorCount;
+    ws->caps = *caps;
+    ws->debug_flags = caps->debug_flags;
+    ws->timeout_ns = caps->timeout_ns ? caps->timeout_ns : kDefaultTimeoutNs;
+
+    e = cudaMalloc(&ws->d_status, sizeof(DevStatus));
+    if (e == cudaSuccess) e = cudaMalloc(&ws->d_counters, kCounterWords * 8);
+    if (e == cudaSuccess && caps->K_max > 0) {
+        const int64_t T = ceil_div(caps->M_max, kBM) * ceil_div(caps->N_max, kBN);
+        ws->mask_words = (size_t)T;
+        ws->part_bytes = (size_t)caps->R_max * (size_t)T * kTilePartBytes;
+        ws->piece_words = (size_t)T * kPieceWords;
+        e = cudaMalloc(&ws->d_mask, ws->mask_words * 4);
+        if (e == cudaSuccess) e = cudaMalloc(&ws->d_part, ws->part_bytes);
+        if (e == cudaSuccess) e = cudaMalloc(&ws->d_pieces, ws->piece_words * 4);
+        if (e == cudaSuccess) e = gemm_prepare_kernels();
+    }
+    if (e == cudaSuccess && caps->N_max <= 32768) {
+        ws->staging_words = (size_t)caps->M_max * (size_t)caps->N_max;
+        e = cudaMalloc(&ws->d_staging, ws->staging_words * 4);
+    }
+    if (e == cudaSuccess) {
+        for (int ppt = 1; ppt <= 16; ppt <<= 1) ws->ar_resident[ppt] = ar_rmsnorm_resident_blocks(ppt, ws->num_sms);
+    }
+    if (e != cudaSuccess) {
+        are_status st = from_cuda(e);
+        free_ws(ws);
+        return st;
+    }
+    are_status st = arm_workspace(ws);
+    if (st != ARE_OK) {
+        free_ws(ws);
+        return st;
+    }
+    *out = ws;
+    return ARE_OK;
+}
+
+are_status are_workspace_destroy(are_ws* ws) {
+    if (!ws) return ARE_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    free_ws(ws);
+    return from_cuda(e);
+}
+
+are_status are_workspace_reset(are_ws* ws) {
+    if (!ws) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    return arm_workspace(ws);
+}
+
+are_status are_workspace_set_debug(are_ws* ws, uint32_t flags, int64_t arg) {
+    if (!ws) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    ws->debug_flags = flags;
+    ws->debug_arg = arg;
+    return ARE_OK;
+}
+
+are_status are_get_device_status(are_ws* ws, are_dev_status* out) {
+    if (!ws || !out) return ARE_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    DevStatus d;
+    e = cudaMemcpy(&d, ws->d_status, sizeof(d), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    out->code = d.code;
+    out->where = d.where;
+    out->a = d.a;
+    out->b = d.b;
+    return d.code == ARE_DEV_OK ? ARE_OK : ARE_ETIMEOUT;
+}
+
+are_status are_debug_snapshot(are_ws* ws, int kind, void* host_dst, size_t bytes) {
+    if (!ws || !host_dst) return ARE_EINVAL;
+    const void* src = nullptr;
+    size_t avail = 0;
+    switch (kind) {
+        case ARE_SNAP_MASKS: src = ws->d_mask; avail = ws->mask_words * 4; break;
+        case ARE_SNAP_STAGING: src = ws->d_staging; avail = ws->staging_words * 4; break;
+        case ARE_SNAP_PIECES: src = ws->d_pieces; avail = ws->piece_words * 4; break;
+        case ARE_SNAP_COUNTERS: src = ws->d_counters; avail = kCounterWords * 8; break;
+        default: return ARE_EINVAL;
+    }
+    if (!src || bytes > avail) return ARE_EINVAL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(host_dst, src, bytes, cudaMemcpyDeviceToHost);
+    return from_cuda(e);
+}
+
+are_status are_gemm_rs(const are_bf16* const A[], const are_bf16* const B[], are_bf16* const out[], int R,
+                       int64_t M, int64_t N, int64_t K, are_ws* ws, void* stream) {
+    return gemm_call(kModeRS, A, B, out, R, M, N, K, ws, stream);
+}
+
+are_status are_gemm_ar(const are_bf16* const A[], const are_bf16* const B[], are_bf16* const out[], int R,
+                       int64_t M, int64_t N, int64_t K, are_ws* ws, void* stream) {
+    return gemm_call(kModeAR, A, B, out, R, M, N, K, ws, stream);
+}
+
+are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
+                                 float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream) {
+    if (!ws || !partials) return ARE_EINVAL;
+    are_status st = are_supports(ARE_OP_ALLREDUCE_RMSNORM, R, M, N, 0);
+    if (st != ARE_OK) return st;
+    for (int r = 0; r < R; ++r)
+        if (!ptr_ok(partials[r], M * N)) return ARE_EINVAL;
+    if ((residual && !aligned16(residual)) || !ptr_ok(gamma, N) || !ptr_ok(out, M * N)) return ARE_EINVAL;
+    if (!(eps > 0.f) || !std::isfinite(eps)) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    if (R > ws->caps.R_max || M > ws->caps.M_max || N > ws->caps.N_max || !ws->d_staging ||
+        (size_t)M * (size_t)N > ws->staging_words)
+        return ARE_ECAPACITY;
+    if (M == 0 || N == 0) return ARE_OK;
+
+    ArParams p;
+    std::memset(&p, 0, sizeof(p));
+    for (int r = 0; r < R; ++r) p.x[r] = partials[r];
+    p.residual = residual;
+    p.gamma = gamma;
+    p.out = out;
+    p.staging = ws->d_staging;
+    p.status = ws->d_status;
+    p.counters = ws->d_counters;
+    p.R = R;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.packs_per_row = (int)(N / 8);
+    int ppt = 1;
+    while (ppt * kArThreads < p.packs_per_row) ppt <<= 1;
+    const int resident = ws->ar_resident[ppt];
+    if (resident <= 0) return ARE_ECUDA;
+    const int grid = std::min(resident, 2 * ws->num_sms);
+    p.chunk_rows = grid;
+    p.num_chunks = (int)ceil_div(M, grid);
+    p.eps = eps;
+    p.inv_n = 1.0f / (float)N;
+    p.flags = ws->debug_flags;
+    p.debug_arg = ws->debug_arg;
+    p.timeout_ns = ws->timeout_ns;
+    ws->last_ar_M = M;
+    ws->last_ar_N = N;
+    return from_cuda(launch_ar_rmsnorm(p, ppt, grid, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/are.h"
+
+namespace are {
+
+constexpr int kMaxRanks = 8;
+
+// Device status word: first error wins (code 0 = no error).
+struct DevStatus {
+    uint32_t code;
+    uint32_t where;
+    int32_t a;
+    int32_t b;
+};
+
+__device__ __forceinline__ void record_error(DevStatus* st, uint32_t code, uint32_t where, int32_t a, int32_t b) {
+    if (atomicCAS(&st->code, 0u, code) == 0u) {
+        st->where = where;
+        st->a = a;
+        st->b = b;
+        __threadfence();
+    }
+}
+
+// ------------------------------------------------------------------ AR+RMSNorm
+constexpr uint32_t kSentinelF32 = 0x80000000u;  // -0.0 as an fp32 word
+constexpr int kArThreads = 256;
+
+struct ArParams {
+    const uint16_t* x[kMaxRanks];  // R bf16 partials [M, N]
+    const uint16_t* residual;      // bf16 [M, N] or nullptr
+    const float* gamma;            // fp32 [N]
+    uint16_t* out;                 // bf16 [M, N]
+    uint32_t* staging;             // fp32 words [M, N], armed with the sentinel
+    DevStatus* status;
+    unsigned long long* counters;  // debug counters
+    int R;
+    int M;
+    int N;
+    int packs_per_row;  // N / 8
+    int chunk_rows;     // rows per pipeline chunk (<= grid)
+    int num_chunks;
+    float eps;
+    float inv_n;
+    uint32_t flags;
+    int64_t debug_arg;
+    uint64_t timeout_ns;
+};
+
+// Largest grid that is fully co-resident for the packs-per-thread variant `ppt`.
+int ar_rmsnorm_resident_blocks(int ppt, int num_sms);
+cudaError_t launch_ar_rmsnorm(const ArParams& p, int ppt, int grid, cudaStream_t stream);
+// Fill n 32-bit words with v.
+cudaError_t launch_fill_u32(uint32_t* dst, uint32_t v, size_t n, cudaStream_t stream);
+
+// ------------------------------------------------------------------ GEMM + reduce
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 3;            // mainloop shared-memory stages
+constexpr int kPStages = 3;           // partial_buf stages
+constexpr int kSubBytes = 16384;      // one 128-row x 128-byte sub-tile
+constexpr int kTilePartBytes = 131072;  // fp32 128x256 partial (bf16 uses the first half)
+constexpr int kGemmThreads = 256;
+constexpr int kPieceWords = 64;       // debug piece log words per tile
+
+enum GemmMode : int { kModeRS = 0, kModeAR = 1 };
+
+struct GemmParams {
+    CUtensorMap tmA[kMaxRanks];
+    CUtensorMap tmB[kMaxRanks];
+    CUtensorMap tmOut[kMaxRanks];
+    uint8_t* part;       // [R][T][tile part bytes]
+    uint32_t* mask;      // [T]
+    DevStatus* status;
+    int32_t* pieces;     // debug piece log [T][kPieceWords]
+    int R;
+    int M, N, K;
+    int S;               // owner segment rows (RS)
+    int H;               // output box height (RS)
+    int nviews;          // distinct output views (AR)
+    int tiles_m, tiles_n, num_tiles, num_units, num_kb;
+    int group_m;         // tile raster: rows of tiles per group
+    uint32_t flags;
+    int64_t debug_arg;
+    uint64_t timeout_ns;
+};
+
+size_t gemm_smem_bytes();
+cudaError_t gemm_prepare_kernels();
+// bf16 [outer, inner] row-major tensor map, 128B-swizzled boxes of box_inner x box_outer.
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                           uint32_t box_outer);
+cudaError_t launch_gemm_reduce(const GemmParams& p, int mode, int grid, cudaStream_t stream);
+
+}  // namespace are

@@ -1,0 +1,574 @@
+// Per-rank partial BF16 GEMMs on the 5th-generation tensor cores, reduced
+// across the R emulated ranks by a bitmask-gated epilogue.
+//
+// Method: DeepGEMM PR #1 "Fused ring RS: per-tile bitmask + drain-ring with
+// owner-boundary flush", description.  Its three points, as built here:
+//   * readiness is a per-tile bitmask (bit r of word t = rank r's partial of
+//     output tile t is in memory), not one flag per owner segment, so a
+//     reducer starts on a tile as soon as that tile's R-1 peer partials exist;
+//   * the peer partials reach the reducer through a multi-stage shared-memory
+//     partial buffer fed by its own loader warp (the page's 2-stage buffer
+//     could not hide the load latency and backed up into TMEM and the MMA);
+//   * outputs leave through asynchronous TMA/bulk stores that are never
+//     drained per tile by the whole epilogue: each staging buffer belongs to
+//     one lane, which waits only for its own bulk group before reusing it
+//     (DeepEP PR #527 "Fix the MultiStages for intranode combine", one stage
+//     per lane), and a producer's publish waits only in the two issuing lanes.
+// The page's title also names an owner-boundary flush: a reduced tile whose
+// rows span several owner segments is cut at the segment boundaries and each
+// piece is stored into its owner's segment.
+//
+// One-GPU design.  A work unit is (rank r, output tile t), a 128x256 tile of
+// P_r = A_r B_r with K = K_r.  Units are ordered tile-major with the tile's
+// reducer (the owner of the tile's first row for GEMM+RS, rank t mod R for
+// GEMM+AR) last among its R units; a persistent grid (one CTA per SM) walks
+// the units wave by wave, CTA b taking unit i*G + (b+i) mod G of wave i, so
+// every wait points at a smaller unit index and the reducers rotate over the
+// CTAs.  Non-reducer units store their partial tile (fp32 for RS, bf16 for AR)
+// into the workspace and release-OR their bit; the reducer keeps its own
+// partial in TMEM, waits (bounded) for the peers' bits, streams their
+// sub-tiles through the partial buffer and adds all R in the order
+// r = 0..R-1 in fp32.
+//
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2
+// TMEM allocator + partial loader, warp 3 idle, warps 4-7 epilogue (TMEM lane
+// = tile row).  TMEM holds two 128x256 fp32 accumulators (512 columns).
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "are_internal.h"
+#include "ptx.cuh"
+
+namespace are {
+namespace {
+
+constexpr uint32_t kAStageBytes = kBM * kBK * 2;  // 16 KB, K-major, 128B-swizzled
+constexpr uint32_t kBStageBytes = kBN * kBK * 2;  // 32 KB, 4 boxes of 64(N) x 64(K), 128B-swizzled
+constexpr uint32_t kStageTx = kAStageBytes + kBStageBytes;
+constexpr int kNumBars = 2 * kStages + 4 + 2 * kPStages + 1;
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * (kAStageBytes + kBStageBytes) + (size_t)kPStages * kSubBytes +
+                              2 * (size_t)kSubBytes + kNumBars * 8 + 16;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// tcgen05 instruction descriptor (kind::f16): D fp32, A bf16, B bf16, A K-major,
+// B MN-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+// Shared-memory matrix descriptor: 128B swizzle, tcgen05 version bit.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+struct Unit {
+    int t, r, own, tm, tn;
+    bool reducer;
+};
+
+__device__ __forceinline__ Unit decode(const GemmParams& p, int mode, int u) {
+    Unit U;
+    U.t = u / p.R;
+    const int j = u - U.t * p.R;
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = U.t / per_group;
+    const int first = g * p.group_m;
+    const int gm = min(p.tiles_m - first, p.group_m);
+    const int in = U.t - g * per_group;
+    U.tm = first + in % gm;
+    U.tn = in / gm;
+    U.own = (mode == kModeRS) ? (U.tm * kBM) / p.S : U.t % p.R;
+    int r = U.own + 1 + j;
+    while (r >= p.R) r -= p.R;
+    U.r = r;
+    U.reducer = (j == p.R - 1);
+    return U;
+}
+
+// Unit of wave i for CTA b: i*G + (b+i) mod G (a rotation per wave).
+__device__ __forceinline__ int unit_of(int b, int i, int G) { return i * G + (b + i) % G; }
+
+// Bounded wait on an mbarrier phase; gives up when the CTA aborts or the
+// workspace timeout expires (recording the error).
+__device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                      const GemmParams& p, int id, int unit) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            record_error(p.status, ARE_DEV_PIPE_TIMEOUT, blockIdx.x, id, unit);
+            *abort_flag = 1u;
+            return false;
+        }
+    }
+}
+
+// Wait for an asynchronous copy that was already issued (it completes on its
+// own); bounded, ignores the abort flag.
+__device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, const GemmParams& p) {
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > p.timeout_ns) break;
+    }
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Epilogue-wide OR of a predicate (uniform result for all 128 threads).
+__device__ __forceinline__ bool epi_bar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// One 128-byte row of a 128B-swizzled 128-row sub-tile: 16-byte chunk c of row
+// `row` lives at chunk position c ^ (row & 7).
+__device__ __forceinline__ void write_row_sw128(uint8_t* base, int row, const uint32_t (&w)[32]) {
+    uint8_t* rp = base + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(rp + ((c ^ (row & 7)) << 4)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+__device__ __forceinline__ void read_row_sw128(const uint8_t* base, int row, uint32_t (&w)[32]) {
+    const uint8_t* rp = base + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & 7)) << 4));
+        w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kStages * kAStageBytes;
+    uint8_t* sP = sB + kStages * kBStageBytes;
+    uint8_t* sOut = sP + kPStages * kSubBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 2 * kSubBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* pfull = tempty + 2;
+    uint64_t* pempty = pfull + kPStages;
+    uint64_t* mma_done = pempty + kPStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const int b = blockIdx.x;
+    const int nsub = (MODE == kModeRS) ? 8 : 4;  // 16 KB sub-tiles per partial tile
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
+        for (int s = 0; s < 2; ++s) { ptx::mbar_init(&tfull[s], 1); ptx::mbar_init(&tempty[s], 128); }
+        for (int s = 0; s < kPStages; ++s) { ptx::mbar_init(&pfull[s], 1); ptx::mbar_init(&pempty[s], 128); }
+        ptx::mbar_init(mma_done, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_shared();
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc(tmem_slot, 512);
+        ptx::tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int r = 0; r < p.R; ++r) { ptx::prefetch_tmap(&p.tmA[r]); ptx::prefetch_tmap(&p.tmB[r]); }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_normal();
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0, issued_ph = 0;  // bit s: stage s has a fill in flight; its parity
+            for (int i = 0;; ++i) {
+                if (i * G >= p.num_units) break;
+                const int u = unit_of(b, i, G);
+                if (u >= p.num_units) continue;
+                const Unit U = decode(p, MODE, u);
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(&empty[stage], ph ^ 1u, abort_flag, p, 0, u)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&full[stage], kStageTx);
+                    ptx::tma_load_2d(sA + stage * kAStageBytes, &p.tmA[U.r], &full[stage], kb * kBK, U.tm * kBM, pol);
+#pragma unroll
+                    for (int q = 0; q < kBN / 64; ++q)
+                        ptx::tma_load_2d(sB + stage * kBStageBytes + q * 8192, &p.tmB[U.r], &full[stage],
+                                         U.tn * kBN + q * 64, kb * kBK, pol);
+                    issued |= 1u << stage;
+                    issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
+                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+            }
+            for (int s = 0; s < kStages; ++s)
+                if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int i = 0;; ++i) {
+                if (i * G >= p.num_units) break;
+                const int u = unit_of(b, i, G);
+                if (u >= p.num_units) continue;
+                const int buf = it & 1;
+                const uint32_t tph = (it >> 1) & 1;
+                if (!wait_bar(&tempty[buf], tph ^ 1u, abort_flag, p, 1, u)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + buf * kBN;
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(&full[stage], ph, abort_flag, p, 2, u)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = ptx::smem_u32(sA + stage * kAStageBytes);
+                    const uint32_t b0 = ptx::smem_u32(sB + stage * kBStageBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        ptx::umma_bf16(d, sdesc(a0 + kk * 32, 16, 1024), sdesc(b0 + kk * 2048, 8192, 1024), kIdesc,
+                                       (kb | kk) != 0);
+                    ptx::umma_commit(&empty[stage]);
+                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::umma_commit(&tfull[buf]);
+                ++it;
+            }
+            // every MMA this thread issued has completed once mma_done flips
+            ptx::umma_commit(mma_done);
+            drain_bar(mma_done, 0, p);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ partial loader
+        if (lane == 0) {
+            int ps = 0;
+            uint32_t pph = 0;
+            uint32_t issued = 0, issued_ph = 0;
+            const uint32_t full_mask = (p.R >= 32) ? 0xFFFFFFFFu : ((1u << p.R) - 1u);
+            for (int i = 0;; ++i) {
+                if (i * G >= p.num_units) break;
+                const int u = unit_of(b, i, G);
+                if (u >= p.num_units) continue;
+                const Unit U = decode(p, MODE, u);
+                if (!U.reducer) continue;
+                const uint32_t need = full_mask & ~(1u << U.own);
+                bool ok = true;
+                if (need) {
+                    uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
+                    if ((seen & need) != need) {
+                        const uint64_t t0 = ptx::globaltimer();
+                        while (true) {
+                            ptx::nanosleep(100);
+                            seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
+                            if ((seen & need) == need) break;
+                            if (*abort_flag || ptx::ld_relaxed_gpu(&p.status->code) != 0u) {
+                                *abort_flag = 1u;
+                                ok = false;
+                                break;
+                            }
+                            if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                                record_error(p.status, ARE_DEV_MASK_TIMEOUT, blockIdx.x, U.t, (int32_t)seen);
+                                *abort_flag = 1u;
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
+                    // generic-proxy acquire above, async-proxy (bulk copy) reads below
+                    ptx::fence_proxy_async_global();
+                }
+                if (!ok) break;
+                for (int j = 0; j < nsub && ok; ++j) {
+                    for (int q = 0; q < p.R; ++q) {
+                        if (q == U.own) continue;
+                        if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 3, u)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&pfull[ps], kSubBytes);
+                        const uint8_t* src =
+                            p.part + ((size_t)q * p.num_tiles + U.t) * kTilePartBytes + (size_t)j * kSubBytes;
+                        ptx::bulk_load(sP + ps * kSubBytes, src, kSubBytes, &pfull[ps]);
+                        issued |= 1u << ps;
+                        issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                        if (++ps == kPStages) { ps = 0; pph ^= 1u; }
+                    }
+                }
+                if (!ok) break;
+            }
+            for (int s = 0; s < kPStages; ++s)
+                if (issued & (1u << s)) drain_bar(&pfull[s], (issued_ph >> s) & 1u, p);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ epilogue
+        const int row = threadIdx.x - 128;  // tile row == TMEM lane
+        const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+        const bool lead = (warp == 4);
+        int it = 0, ps = 0;
+        uint32_t pph = 0;
+        bool bad = false;
+        for (int i = 0;; ++i) {
+            if (i * G >= p.num_units) break;
+            const int u = unit_of(b, i, G);
+            if (u >= p.num_units) continue;
+            const Unit U = decode(p, MODE, u);
+            const int buf = it & 1;
+            const uint32_t tph = (it >> 1) & 1;
+            if (!wait_bar(&tfull[buf], tph, abort_flag, p, 4, u)) bad = true;
+            ptx::tc_fence_after();
+            __syncwarp();
+            const uint32_t tacc = tmem_base + lane_base + buf * kBN;
+            const int row0 = U.tm * kBM;
+
+            if (!U.reducer) {
+                // ---- producer unit: TMEM -> registers -> swizzled smem -> bulk store -> publish
+                uint8_t* gdst = p.part + ((size_t)U.r * p.num_tiles + U.t) * kTilePartBytes;
+                for (int j = 0; j < nsub; ++j) {
+                    uint32_t w[32];
+                    if (MODE == kModeRS) {
+                        ptx::tmem_ld32(tacc + j * 32, w);
+                    } else {
+                        uint32_t v0[32], v1[32];
+                        ptx::tmem_ld32(tacc + j * 64, v0);
+                        ptx::tmem_ld32(tacc + j * 64 + 32, v1);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            w[c] = pack_bf16x2(__uint_as_float(v0[2 * c]), __uint_as_float(v0[2 * c + 1]));
+                            w[16 + c] = pack_bf16x2(__uint_as_float(v1[2 * c]), __uint_as_float(v1[2 * c + 1]));
+                        }
+                    }
+                    if (j == nsub - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(&tempty[buf]);
+                    }
+                    const int sb = j & 1;
+                    if (lead && lane == sb) ptx::bulk_wait_read0();
+                    if (epi_bar_or(bad)) { bad = true; break; }
+                    write_row_sw128(sOut + sb * kSubBytes, row, w);
+                    ptx::fence_proxy_async_shared();
+                    epi_bar();
+                    if (lead && lane == sb) {
+                        ptx::bulk_store(gdst + (size_t)j * kSubBytes, sOut + sb * kSubBytes, kSubBytes);
+                        ptx::bulk_commit();
+                    }
+                }
+                if (bad) break;
+                if (lead) {
+                    if (lane < 2) {
+                        ptx::bulk_wait0();
+                        ptx::fence_proxy_async_global();
+                        __threadfence();
+                    }
+                    __syncwarp();
+                    if (lane == 0 && !((p.flags & ARE_DEBUG_SKIP_PUBLISH) && (int64_t)u == p.debug_arg))
+                        ptx::red_release_or(&p.mask[U.t], 1u << U.r);
+                }
+            } else {
+                // ---- reducer unit: own partial in TMEM + R-1 peers through partial_buf
+                if (lead && lane == 0) ptx::red_relaxed_or(&p.mask[U.t], 1u << U.own);
+                for (int c = 0; c < kBN / 64; ++c) {  // 64-column output chunks
+                    uint32_t outw[32];
+                    if (MODE == kModeRS) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int j = 2 * c + h;
+                            float acc[32];
+                            for (int q = 0; q < p.R; ++q) {
+                                uint32_t v[32];
+                                if (q == U.own) {
+                                    __syncwarp();
+                                    ptx::tmem_ld32(tacc + j * 32, v);
+                                } else {
+                                    if (!wait_bar(&pfull[ps], pph, abort_flag, p, 5, u)) bad = true;
+                                    read_row_sw128(sP + ps * kSubBytes, row, v);
+                                    ptx::mbar_arrive(&pempty[ps]);
+                                    if (++ps == kPStages) { ps = 0; pph ^= 1u; }
+                                }
+                                if (q == 0) {
+#pragma unroll
+                                    for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(v[e]);
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 32; ++e) acc[e] = acc[e] + __uint_as_float(v[e]);
+                                }
+                            }
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) outw[16 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+                        }
+                    } else {
+                        const int j = c;
+                        float acc[64];
+                        for (int q = 0; q < p.R; ++q) {
+                            uint32_t v[32];  // 64 bf16
+                            if (q == U.own) {
+                                uint32_t t0[32], t1[32];
+                                __syncwarp();
+                                ptx::tmem_ld32(tacc + j * 64, t0);
+                                ptx::tmem_ld32(tacc + j * 64 + 32, t1);
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    v[e] = pack_bf16x2(__uint_as_float(t0[2 * e]), __uint_as_float(t0[2 * e + 1]));
+                                    v[16 + e] = pack_bf16x2(__uint_as_float(t1[2 * e]), __uint_as_float(t1[2 * e + 1]));
+                                }
+                            } else {
+                                if (!wait_bar(&pfull[ps], pph, abort_flag, p, 5, u)) bad = true;
+                                read_row_sw128(sP + ps * kSubBytes, row, v);
+                                ptx::mbar_arrive(&pempty[ps]);
+                                if (++ps == kPStages) { ps = 0; pph ^= 1u; }
+                            }
+                            if (q == 0) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) {
+                                    acc[2 * e] = __uint_as_float(v[e] << 16);
+                                    acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) {
+                                    acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
+                                    acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) outw[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+                    }
+                    if (c == kBN / 64 - 1) {
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(&tempty[buf]);
+                    }
+                    const int sb = c & 1;
+                    if (lead && lane == sb) ptx::bulk_wait_read0();
+                    if (epi_bar_or(bad)) { bad = true; break; }
+                    write_row_sw128(sOut + sb * kSubBytes, row, outw);
+                    ptx::fence_proxy_async_shared();
+                    epi_bar();
+                    if (lead && lane == sb) {
+                        const int x = U.tn * kBN + c * 64;
+                        if (x < p.N) {
+                            if (MODE == kModeRS) {
+                                // owner-boundary flush: one store per (segment piece, H-row box)
+                                const int row_end = min(row0 + kBM, p.M);
+                                for (int r0 = row0; r0 < row_end;) {
+                                    const int s = r0 / p.S;
+                                    const int e = min((s + 1) * p.S, row_end);
+                                    for (int rb = r0; rb < e; rb += p.H)
+                                        ptx::tma_store_2d(&p.tmOut[s], sOut + sb * kSubBytes + (rb - row0) * 128, x,
+                                                          rb - s * p.S);
+                                    r0 = e;
+                                }
+                            } else {
+                                for (int v = 0; v < p.nviews; ++v)
+                                    ptx::tma_store_2d(&p.tmOut[v], sOut + sb * kSubBytes, x, row0);
+                            }
+                            ptx::bulk_commit();
+                        }
+                    }
+                }
+                if (bad) break;
+                if (lead && lane == 0) {
+                    if (MODE == kModeRS && (p.flags & ARE_DEBUG_LOG_PIECES)) {
+                        int32_t* log = p.pieces + (size_t)U.t * kPieceWords;
+                        const int row_end = min(row0 + kBM, p.M);
+                        int n = 0;
+                        for (int r0 = row0; r0 < row_end && n < (kPieceWords - 3) / 3;) {
+                            const int s = r0 / p.S;
+                            const int e = min((s + 1) * p.S, row_end);
+                            log[3 + 3 * n] = s; log[4 + 3 * n] = r0; log[5 + 3 * n] = e;
+                            ++n;
+                            r0 = e;
+                        }
+                        log[0] = U.tm; log[1] = U.tn; log[2] = n;
+                    }
+                    // re-arm the tile's mask word for the next call
+                    if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
+                }
+            }
+            ++it;
+        }
+        if (bad) *abort_flag = 1u;
+        if (lead && lane < 2) ptx::bulk_wait0();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 2) {
+        __syncwarp();
+        ptx::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+cudaError_t get_encode() {
+    std::lock_guard<std::mutex> lk(g_encode_mu);
+    if (g_encode) return cudaSuccess;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t gemm_prepare_kernels() {
+    cudaError_t e = cudaFuncSetAttribute(gemm_reduce_kernel<kModeRS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_reduce_kernel<kModeAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return get_encode();
+}
+
+// bf16 [outer, inner] row-major, 128B-swizzled boxes of box_inner x box_outer.
+cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                           uint32_t box_outer) {
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_reduce(const GemmParams& p, int mode, int grid, cudaStream_t stream) {
+    if (mode == kModeRS)
+        gemm_reduce_kernel<kModeRS><<<grid, kGemmThreads, kSmemBytes, stream>>>(p);
+    else
+        gemm_reduce_kernel<kModeAR><<<grid, kGemmThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace are

@@ -1,0 +1,219 @@
+/*
+ * are.h — C ABI of the GB300 (sm_103a) tensor-parallel row-parallel linear
+ * epilogue library (libare.so).
+ *
+ * The operations, with the pages that define them:
+ *
+ *  are_gemm_rs   R per-rank partial BF16 GEMMs P_r = A_r[M,K] x B_r[K,N]
+ *                (fp32 accumulation), summed in the fixed ring order
+ *                r = 0..R-1 and reduce-scattered: rank s receives rows
+ *                [s*M/R, (s+1)*M/R) of bf16(sum).  DeepGEMM PR #1 "Fused ring
+ *                RS: per-tile bitmask + drain-ring with owner-boundary flush",
+ *                description (fused BF16 GEMM + reduce-scatter; per-tile ready
+ *                bitmask instead of a per-segment flag; multi-stage partial
+ *                buffer; asynchronous TMA stores not drained per tile).
+ *  are_gemm_ar   The same R partial GEMMs, each rounded to a bf16 output, then
+ *                all-reduced (fp32 sum in ring order, rounded to bf16) into
+ *                every rank's view.  ROCm/mori PR #662 "Fuse DSV4-Pro wo_b's
+ *                GEMM with its all-reduce", description (GEMM whose bf16
+ *                [M, 7168] output is all-reduced across TP ranks).
+ *  are_allreduce_rmsnorm
+ *                All-reduce of R bf16 partials, residual add and RMSNorm in
+ *                one kernel whose two phases meet through a staging buffer
+ *                armed with the -0.0 sentinel (the data is its own flag).
+ *                ROCm/aiter PR #4977 "Single-kernel Lamport fused all-reduce +
+ *                RMSNorm", sections "Approach" and "Correctness notes".
+ *
+ * On one GPU the R ranks are R separate device buffers; the library emulates
+ * their exchange in HBM/L2 and uses no collective.
+ *
+ * Conventions
+ *  - All tensors are row-major and owned by the caller; every tensor pointer
+ *    is a DEVICE pointer, 16-byte aligned.  Arrays of per-rank pointers
+ *    (A[], B[], out[], partials[]) are HOST arrays of R device pointers; the
+ *    library copies them before the call returns.
+ *  - `are_bf16` is the 16-bit pattern of a bfloat16 (upper half of an IEEE
+ *    binary32).  bf16 results are rounded to nearest even.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are asynchronous and stream-ordered; they launch kernels
+ *    and never synchronise.  A workspace must be used from one stream at a
+ *    time: calls on different streams with the same workspace race on the
+ *    device, and a call made while another host thread is inside the library
+ *    with the same workspace returns ARE_EBUSY.
+ *  - Every argument is validated before anything is launched: on any error
+ *    nothing is launched and nothing is written.
+ *  - Device-side waits are bounded by the workspace's timeout.  A wait that
+ *    expires records an error in the workspace's device status word, makes
+ *    every other wait of that workspace give up, and lets the kernel return;
+ *    read it with are_get_device_status().  After such an error the outputs
+ *    of that call are undefined and the workspace must be re-armed with
+ *    are_workspace_reset() before further use (until then every call aborts
+ *    at its first wait).
+ */
+#ifndef ARE_H
+#define ARE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ARE_API __attribute__((visibility("default")))
+#else
+#define ARE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t are_bf16;
+
+typedef enum are_status {
+    ARE_OK = 0,
+    ARE_EINVAL = 1,   /* bad argument: NULL or misaligned pointer, size outside are_supports(), eps <= 0 ... */
+    ARE_ENOMEM = 2,   /* device allocation failed (workspace creation only) */
+    ARE_ECUDA = 3,    /* a CUDA runtime call or kernel launch failed */
+    ARE_ETIMEOUT = 4, /* a bounded device wait expired (reported by are_get_device_status) */
+    ARE_EBUSY = 5,    /* the workspace is in use by another host thread */
+    ARE_ENODEV = 6,   /* the current device is not an sm_103 GPU */
+    ARE_ECAPACITY = 7 /* the call exceeds the capacities the workspace was created with */
+} are_status;
+
+typedef enum are_op {
+    ARE_OP_GEMM_RS = 1,
+    ARE_OP_GEMM_AR = 2,
+    ARE_OP_ALLREDUCE_RMSNORM = 3
+} are_op;
+
+/* Workspace capacities.  Buffers are sized from these once, at creation, so
+ * their layout never moves with the shapes of later calls. */
+typedef struct are_caps {
+    int32_t R_max;       /* largest R, 1..8 */
+    int64_t M_max;       /* largest M */
+    int64_t N_max;       /* largest N */
+    int64_t K_max;       /* largest K; 0 = no GEMM buffers (AR+RMSNorm only) */
+    uint64_t timeout_ns; /* bound of every device-side wait; 0 = 200 ms */
+    uint32_t debug_flags;/* ARE_DEBUG_* */
+    uint32_t reserved;
+} are_caps;
+
+/* Debug switches (default off; they change bookkeeping, never the arithmetic). */
+enum {
+    ARE_DEBUG_NO_REARM = 1u,      /* keep tile masks / staging words as the call left them (snapshots) */
+    ARE_DEBUG_LOG_PIECES = 2u,    /* record the owner pieces each GEMM+RS reducer stored */
+    ARE_DEBUG_COUNT_CANON = 4u,   /* count staged words canonicalised from -0.0 to +0.0 */
+    ARE_DEBUG_SKIP_PUBLISH = 8u,  /* GEMM: work unit `debug_arg` never sets its ready bit */
+    ARE_DEBUG_SKIP_STAGE = 16u    /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
+};
+
+/* Device status word, see are_get_device_status(). */
+typedef struct are_dev_status {
+    uint32_t code;  /* ARE_DEV_* */
+    uint32_t where; /* block index that recorded it */
+    int32_t a;      /* MASK_TIMEOUT: tile; STAGE_TIMEOUT: row; PIPE_TIMEOUT: barrier id */
+    int32_t b;      /* MASK_TIMEOUT: mask word seen; STAGE_TIMEOUT: pack in row; PIPE_TIMEOUT: unit */
+} are_dev_status;
+
+enum {
+    ARE_DEV_OK = 0,
+    ARE_DEV_MASK_TIMEOUT = 1,  /* a GEMM reducer waited too long for a tile's ready bits */
+    ARE_DEV_STAGE_TIMEOUT = 2, /* an RMSNorm consumer waited too long for a staged pack */
+    ARE_DEV_PIPE_TIMEOUT = 3   /* a GEMM pipeline barrier wait expired */
+};
+
+/* Snapshot kinds for are_debug_snapshot(). */
+enum {
+    ARE_SNAP_MASKS = 1,    /* uint32 per tile (tile index in the kernel's work order) */
+    ARE_SNAP_STAGING = 2,  /* fp32 staging words, row-major [M, N] of the last AR+RMSNorm call */
+    ARE_SNAP_PIECES = 3,   /* int32 x 64 per tile: tile_m, tile_n, count, then (segment, begin, end) x count */
+    ARE_SNAP_COUNTERS = 4  /* uint64 x 4: [0] canonicalised words */
+};
+
+typedef struct are_ws are_ws;
+
+/* Library version, (major << 16) | minor. */
+ARE_API int are_version(void);
+
+/* Human-readable name of a status code (static string). */
+ARE_API const char* are_status_string(are_status s);
+
+/* The predicate every call applies before launching; ARE_OK if supported.
+ *  GEMM_RS: 1 <= R <= 8; M, N >= 0; K >= 0; K % 8 == 0 and N % 8 == 0 (16-byte
+ *           rows for TMA); M % R == 0 and (M / R) % 8 == 0 (owner segments
+ *           start on 8-row boundaries).
+ *  GEMM_AR: 1 <= R <= 8; K % 8 == 0; N % 8 == 0.
+ *  ALLREDUCE_RMSNORM: 1 <= R <= 8; N % 8 == 0 (16-byte packs); N <= 32768.
+ * K is ignored for ALLREDUCE_RMSNORM. */
+ARE_API are_status are_supports(int op, int R, int64_t M, int64_t N, int64_t K);
+
+/* Create a workspace on the current CUDA device: tile masks, the per-rank
+ * partial buffer, the Lamport staging buffer (filled with the sentinel, on a
+ * private stream, synchronously) and the device status word.  On failure
+ * everything acquired so far is released and the first error is returned
+ * (*ws is then NULL).  Must not be called during stream capture. */
+ARE_API are_status are_workspace_create(are_ws** ws, const are_caps* caps);
+
+/* Release a workspace (synchronises the device first).  NULL is accepted. */
+ARE_API are_status are_workspace_destroy(are_ws* ws);
+
+/* Clear the device status word, zero every tile mask and re-arm every staging
+ * word with the sentinel; synchronous.  Needed only after a device error (or
+ * after a debug call made with ARE_DEBUG_NO_REARM).  Not capturable. */
+ARE_API are_status are_workspace_reset(are_ws* ws);
+
+/* Change the debug switches (ARE_DEBUG_*) and their argument for later calls. */
+ARE_API are_status are_workspace_set_debug(are_ws* ws, uint32_t flags, int64_t arg);
+
+/* Synchronise the device, then copy the workspace's device status word.
+ * Returns ARE_ETIMEOUT if a device wait expired, else ARE_OK. */
+ARE_API are_status are_get_device_status(are_ws* ws, are_dev_status* out);
+
+/* Synchronise the device and copy `bytes` of a bookkeeping buffer (ARE_SNAP_*)
+ * to host memory `host_dst`. */
+ARE_API are_status are_debug_snapshot(are_ws* ws, int kind, void* host_dst, size_t bytes);
+
+/*
+ * GEMM + reduce-scatter.
+ *  A[r]   : bf16 [M, K] (K contiguous), r < R
+ *  B[r]   : bf16 [K, N] (N contiguous), r < R
+ *  out[s] : bf16 [M/R, N], rank s's owner segment, s < R.  Passing
+ *           out[s] = base + s*(M/R)*N fills one contiguous [M, N] tensor.
+ *  Result : out[s][i][j] = bf16( sum_{r=0..R-1} P_r[s*M/R + i][j] ), the fp32
+ *           partials added in the order r = 0, 1, ..., R-1.
+ * Outputs must not alias inputs.  K == 0 writes zeros.
+ */
+ARE_API are_status are_gemm_rs(const are_bf16* const A[], const are_bf16* const B[], are_bf16* const out[], int R,
+                       int64_t M, int64_t N, int64_t K, are_ws* ws, void* stream);
+
+/*
+ * GEMM + all-reduce.
+ *  A[r], B[r] as for are_gemm_rs.
+ *  out[v] : bf16 [M, N] for every rank view v < R (views may alias each other;
+ *           identical pointers are written once).
+ *  Result : out[v][i][j] = bf16( sum_{r=0..R-1} f32(bf16(P_r[i][j])) ), in the
+ *           order r = 0..R-1: each rank's GEMM output is bf16 before the
+ *           all-reduce, the sum is fp32.
+ */
+ARE_API are_status are_gemm_ar(const are_bf16* const A[], const are_bf16* const B[], are_bf16* const out[], int R,
+                       int64_t M, int64_t N, int64_t K, are_ws* ws, void* stream);
+
+/*
+ * All-reduce + residual add + RMSNorm (one kernel).
+ *  partials[r] : bf16 [M, N], r < R
+ *  residual    : bf16 [M, N] or NULL (treated as zero)
+ *  gamma       : fp32 [N]
+ *  out         : bf16 [M, N]
+ *  Result      : s = sum_{r=0..R-1} f32(partials[r]) in that order, -0.0
+ *                staged as +0.0; h = s + f32(residual);
+ *                out = bf16( h * rsqrt(mean_j(h_j^2) + eps) * gamma ).
+ * eps must be finite and > 0.  The staging buffer must have been armed (it is
+ * at creation, and every call re-arms what it consumed).
+ */
+ARE_API are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
+                                 float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ARE_H */
