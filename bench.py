@@ -1,0 +1,470 @@
+#!/usr/bin/env python3
+"""Benchmark of the row-parallel linear epilogue hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+
+  gemm_rs            R=8, M=N=8192, K=4096: 8 partial BF16 GEMMs, ring-order
+                     fp32 sum, reduce-scatter into 8 owner segments of 1024 rows
+  gemm_ar            R=8, M=4096, N=7168, K=2048: 8 partial GEMMs rounded to
+                     bf16, all-reduced into 8 rank views
+  allreduce_rmsnorm  R=8 bf16 partials [4096, 7168] (1% -0.0), bf16 residual,
+                     fp32 gamma: Lamport all-reduce + residual + RMSNorm
+
+Every input is larger than the 129 MB L2, so no flush is needed between
+steps.  ``value`` is the step's roofline fraction: the sum over the three
+kernels of max(FLOPs / bf16 peak, algorithmic bytes / HBM bandwidth),
+divided by the measured step time (per GPU; summed over GPUs for N > 1,
+where every rank runs its own replica).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the CPU oracle (the only reference implementation
+that exists for this method) on bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused GEMM+RS TFLOP/s and AR+RMSNorm GB/s on 1 GB300, % of roofline"
+UNIT = "% of one GB300's roofline"
+WORKLOAD = {
+    "gemm_rs": dict(R=8, M=8192, N=8192, K=4096, seed_cfg=4),
+    "gemm_ar": dict(R=8, M=4096, N=7168, K=2048, seed_cfg=2),
+    "allreduce_rmsnorm": dict(R=8, M=4096, N=7168, seed_cfg=3),
+}
+EPS = 1e-6
+# Fallback denominators (one earlier GB300 measurement), used only when the
+# measured peaks file is absent.
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM traffic per launch (read + write bytes) from one ncu capture of each
+# kernel (see profiles/); None until captured for the current kernel source.
+NCU_TRAFFIC = {"gemm_rs": None, "gemm_ar": None, "allreduce_rmsnorm": None}
+
+
+# --------------------------------------------------------------------------- work model
+
+def work(part: str):
+    w = WORKLOAD[part]
+    R, M, N = w["R"], w["M"], w["N"]
+    if part == "allreduce_rmsnorm":
+        return 0.0, float(2 * M * N * (R + 2) + 4 * N)
+    K = w["K"]
+    flops = 2.0 * R * M * N * K
+    if part == "gemm_rs":
+        return flops, float(2 * (R * M * K + R * K * N + M * N))
+    return flops, float(2 * (R * M * K + R * K * N + R * M * N))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = dict(FALLBACK_PEAKS)
+    source = "fallback"
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, f"{pre}{k}.")
+                else:
+                    flat[pre[:-1]] = x
+            walk(d)
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                cands = [v for k, v in flat.items() if k.split(".")[-1] == key and isinstance(v, (int, float))]
+                if cands:
+                    peaks[key] = float(cands[0])
+                    source = "measured"
+        except Exception:
+            pass
+    return peaks, source
+
+
+def roofline_seconds(part: str, peaks) -> float:
+    flops, byts = work(part)
+    return max(flops / (peaks["bf16_tflops_sustained"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+
+
+# --------------------------------------------------------------------------- clocks
+
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={CLOCK_QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+        return dist
+    return None
+
+
+def max_over_ranks(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- inputs
+
+def host_inputs():
+    """Seeded synthetic host inputs (numpy bf16 bit patterns) for one step."""
+    import synth
+    w = WORKLOAD
+    out = {}
+    g = w["gemm_rs"]
+    out["gemm_rs"] = synth.gemm_inputs(g["R"], g["M"], g["N"], g["K"], synth.config_seed(g["seed_cfg"]))
+    g = w["gemm_ar"]
+    out["gemm_ar"] = synth.gemm_inputs(g["R"], g["M"], g["N"], g["K"], synth.config_seed(g["seed_cfg"]))
+    g = w["allreduce_rmsnorm"]
+    out["allreduce_rmsnorm"] = synth.ar_inputs(g["R"], g["M"], g["N"], synth.config_seed(g["seed_cfg"]))
+    return out
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_time(nthreads: int = 0):
+    """Time the oracle as it stands on bounded row samples of each part and
+    extrapolate linearly in rows to one full step.  Returns (seconds per full
+    step, threads used, sample description)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    o = oracle.Oracle(0, nthreads)
+    threads = o.max_threads() if nthreads == 0 else nthreads
+    total = 0.0
+    desc = []
+    for part, nrows in (("gemm_rs", 64), ("gemm_ar", 64)):
+        w = WORKLOAD[part]
+        R, M, N, K = w["R"], w["M"], w["N"], w["K"]
+        # a bounded slice of rows is enough: only those rows of A are drawn
+        rows = np.linspace(0, M - 1, nrows).astype(np.int64)
+        seed = synth.config_seed(w["seed_cfg"])
+        s = 1.0 / np.sqrt(K)
+        A = [synth.normal_bf16((M, K), seed, synth.T_A, r, 0.0, s) for r in range(R)]
+        B = [synth.normal_bf16((K, N), seed, synth.T_B, r, 0.0, s) for r in range(R)]
+        t0 = time.perf_counter()
+        o.gemm_reduce_rows(A, B, rows, "rs" if part == "gemm_rs" else "ar")
+        dt = time.perf_counter() - t0
+        total += dt * M / nrows
+        desc.append(f"{part}: {nrows} of {M} rows in {dt:.2f} s")
+        del A, B
+    w = WORKLOAD["allreduce_rmsnorm"]
+    R, M, N = w["R"], w["M"], w["N"]
+    nrows = 512
+    parts, res, gamma = synth.ar_inputs(R, nrows, N, synth.config_seed(w["seed_cfg"]))
+    t0 = time.perf_counter()
+    o.allreduce_rmsnorm(parts, res, gamma, EPS)
+    dt = time.perf_counter() - t0
+    total += dt * M / nrows
+    desc.append(f"allreduce_rmsnorm: {nrows} of {M} rows in {dt:.3f} s")
+    return total, threads, "; ".join(desc) + "; extrapolated linearly in rows to one full step"
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    peaks, source = load_peaks()
+    roof = sum(roofline_seconds(p, peaks) for p in WORKLOAD)
+    for _ in range(args.warmup):
+        oracle_sample_time()
+    times = []
+    threads, sample = 0, ""
+    for _ in range(args.steps):
+        t, threads, sample = oracle_sample_time()
+        times.append(t)
+    step_s = statistics.mean(times)
+    value = 100.0 * roof / step_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "peaks": {"source": source, **peaks},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_block():
+    return {"workload": "epilogue hot path: gemm_rs R=8 M=N=8192 K=4096 (8 owner segments) + gemm_ar R=8 "
+                        "M=4096 N=7168 K=2048 (8 views) + allreduce_rmsnorm R=8 M=4096 N=7168",
+            "parts": {k: {kk: vv for kk, vv in v.items() if kk != "seed_cfg"} for k, v in WORKLOAD.items()},
+            "parallelism": "replicas (one full step per GPU; the ranks are emulated on each GPU)",
+            "l2": "inputs larger than L2 (each part streams >= 369 MB), no flush"}
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    peaks, source = load_peaks()
+
+    host = host_inputs()
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    wr, wa, wn = WORKLOAD["gemm_rs"], WORKLOAD["gemm_ar"], WORKLOAD["allreduce_rmsnorm"]
+    A_rs = [to_dev(a) for a in host["gemm_rs"][0]]
+    B_rs = [to_dev(b) for b in host["gemm_rs"][1]]
+    A_ar = [to_dev(a) for a in host["gemm_ar"][0]]
+    B_ar = [to_dev(b) for b in host["gemm_ar"][1]]
+    parts_h, res_h, gamma_h = host["allreduce_rmsnorm"]
+    P_n = [to_dev(x) for x in parts_h]
+    res_n = to_dev(res_h)
+    gamma_n = torch.from_numpy(gamma_h).to(dev)
+    out_rs = torch.empty((wr["M"], wr["N"]), dtype=torch.bfloat16, device=dev)
+    out_ar = [torch.empty((wa["M"], wa["N"]), dtype=torch.bfloat16, device=dev) for _ in range(wa["R"])]
+    out_n = torch.empty((wn["M"], wn["N"]), dtype=torch.bfloat16, device=dev)
+    ws = are.Workspace(R_max=8, M_max=max(wr["M"], wa["M"], wn["M"]), N_max=max(wr["N"], wa["N"], wn["N"]),
+                       K_max=max(wr["K"], wa["K"]))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        are.gemm_rs(A_rs, B_rs, out_rs, ws, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        are.gemm_ar(A_ar, B_ar, out_ar, ws, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = ws.device_status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device status after warm-up: {st}")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.3)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    if dist is not None:
+        dist.barrier()
+    st = ws.device_status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device status after timed steps: {st}")
+    total_ms = t_start.elapsed_time(t_end)
+    per = {p: [] for p in WORKLOAD}
+    for ev in events:
+        per["gemm_rs"].append(ev[0].elapsed_time(ev[1]))
+        per["gemm_ar"].append(ev[1].elapsed_time(ev[2]))
+        per["allreduce_rmsnorm"].append(ev[2].elapsed_time(ev[3]))
+    ms_step = max_over_ranks(dist, total_ms / args.steps, dev)
+    per_ms = {p: statistics.mean(v) for p, v in per.items()}
+
+    roof = {p: roofline_seconds(p, peaks) for p in WORKLOAD}
+    value = world * 100.0 * sum(roof.values()) / (ms_step * 1e-3)
+    parts = {}
+    for p in WORKLOAD:
+        flops, byts = work(p)
+        d = {"ms": per_ms[p], "roofline_ms": roof[p] * 1e3, "frac_of_roofline": roof[p] / (per_ms[p] * 1e-3)}
+        if flops:
+            d["tflops"] = flops / (per_ms[p] * 1e-3) / 1e12
+        d["gbs_algorithmic"] = byts / (per_ms[p] * 1e-3) / 1e9
+        parts[p] = d
+    peak_t = peaks["bf16_tflops_sustained"]
+    flops_rs, _ = work("gemm_rs")
+    ach_rs = flops_rs / (per_ms["gemm_rs"] * 1e-3) / 1e12
+    roofline = {"kernel": "gemm_reduce_kernel<RS> (gemm_rs)", "bound": "tensor", "achieved": ach_rs,
+                "peak": peak_t, "unit": "TFLOP/s", "frac": ach_rs / peak_t, "traffic": NCU_TRAFFIC["gemm_rs"],
+                "peak_source": f"{source} bf16 sustained", "note": f"of {source}"}
+    _, bytes_n = work("allreduce_rmsnorm")
+    ach_n = bytes_n / (per_ms["allreduce_rmsnorm"] * 1e-3) / 1e9
+    roofline_ar = {"kernel": "ar_rmsnorm_kernel (allreduce_rmsnorm)", "bound": "hbm", "achieved": ach_n,
+                   "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach_n / peaks["hbm_gbs"],
+                   "traffic": NCU_TRAFFIC["allreduce_rmsnorm"], "peak_source": f"{source} HBM copy",
+                   "note": f"of {source}"}
+
+    # ---- end to end: pinned host inputs -> device, the three calls, results -> host
+    e2e_steps = max(1, min(args.steps, 5))
+    pin = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).pin_memory()  # noqa: E731
+    hA_rs = [pin(a) for a in host["gemm_rs"][0]]
+    hB_rs = [pin(b) for b in host["gemm_rs"][1]]
+    hA_ar = [pin(a) for a in host["gemm_ar"][0]]
+    hB_ar = [pin(b) for b in host["gemm_ar"][1]]
+    hP = [pin(x) for x in parts_h]
+    hres = pin(res_h)
+    hgamma = torch.from_numpy(gamma_h).pin_memory()
+    ho_rs = torch.empty(out_rs.shape, dtype=torch.int16).pin_memory()
+    ho_ar = [torch.empty(o.shape, dtype=torch.int16).pin_memory() for o in out_ar]
+    ho_n = torch.empty(out_n.shape, dtype=torch.int16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hA_rs + hB_rs + hA_ar + hB_ar + hP + [hres, hgamma])
+    d2h = sum(t.numel() * t.element_size() for t in [ho_rs, ho_n] + ho_ar)
+
+    def e2e_step():
+        for h, d in zip(hA_rs + hB_rs + hA_ar + hB_ar + hP + [hres],
+                        A_rs + B_rs + A_ar + B_ar + P_n + [res_n]):
+            d.view(torch.int16).copy_(h, non_blocking=True)
+        gamma_n.copy_(hgamma, non_blocking=True)
+        step()
+        ho_rs.copy_(out_rs.view(torch.int16), non_blocking=True)
+        for h, d in zip(ho_ar, out_ar):
+            h.copy_(d.view(torch.int16), non_blocking=True)
+        ho_n.copy_(out_n.view(torch.int16), non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / e2e_steps, dev)
+    e2e_value = world * 100.0 * sum(roof.values()) / (e2e_ms * 1e-3)
+    st = ws.device_status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device status after e2e steps: {st}")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu_s, threads, sample = oracle_sample_time()
+        cpu = {"value": 100.0 * sum(roof.values()) / cpu_s, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": sample, "ms_per_step_extrapolated": cpu_s * 1e3}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator, shapes of the workloads)",
+            "config": config_block(),
+            "parts": parts,
+            "roofline": roofline,
+            "roofline_allreduce_rmsnorm": roofline_ar,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "steps": e2e_steps},
+            "gpu_launches": 3 * args.steps,
+            "peaks": {"source": source, **peaks},
+        }
+        print(json.dumps(line), flush=True)
+    ws.close()
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        sys.stderr.write("note: fewer than 3 warm-up steps\n")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
