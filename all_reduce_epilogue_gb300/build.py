@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libare.so")
-SOURCES = ["api.cu", "gemm_reduce.cu", "ar_rmsnorm.cu"]
+SOURCES = ["api.cu", "gemm_reduce.cu", "ar_rmsnorm.cu", "noalloc.cu"]
 HEADERS = ["are_internal.h", "ptx.cuh"]
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 

@@ -212,6 +212,38 @@ ARE_API are_status are_gemm_ar(const are_bf16* const A[], const are_bf16* const 
 ARE_API are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
                                  float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream);
 
+/*
+ * All-reduce + residual + RMSNorm that allocates nothing.
+ *
+ * The pages have no counterpart to this entry point.  It is for callers that
+ * cannot let a library call cudaMalloc or cudaFree: a framework whose caching
+ * allocator must own every device byte, a process held to a fixed
+ * device-memory budget, or code that cannot pay the device-wide
+ * synchronisation an allocation or a free can cause.  Such callers cannot
+ * create a workspace, so this call needs none.
+ *
+ *  Arguments and result: as are_allreduce_rmsnorm, without `ws`.
+ *  Scratch: a fixed array compiled into the library (8 MiB of fp32 staging
+ *           words after a 256-byte status header), held by every GPU that
+ *           loads the library until the process exits.
+ *  Limit:   M * N <= 2,097,152 (e.g. M <= 292 at N = 7168); a larger call
+ *           returns ARE_ECAPACITY and launches nothing.
+ *  Set-up:  the first call on a device looks up the array's device address
+ *           (once per device, with that device current); make that first
+ *           call before any stream capture.
+ *  Sharing: every call uses the same array and it keeps the last call's
+ *           contents.  Each call therefore first clears the status word and
+ *           re-arms the staging words it uses with the -0.0 sentinel, on
+ *           `stream`, then runs the kernel.  Calls whose kernels can overlap
+ *           on the GPU (other streams, other host threads) race on the array
+ *           and give undefined results.  A device-side wait that expires is
+ *           not reported by this entry point; the output is then undefined.
+ *  Never calls cudaMalloc, cudaFree or any allocating library routine.
+ */
+ARE_API are_status are_allreduce_rmsnorm_noalloc(const are_bf16* const partials[], const are_bf16* residual,
+                                                 const float* gamma, float eps, are_bf16* out, int R, int64_t M,
+                                                 int64_t N, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
