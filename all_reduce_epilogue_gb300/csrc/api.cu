@@ -35,7 +35,7 @@ struct are_ws {
     size_t piece_words = 0;
     uint32_t* d_staging = nullptr;
     size_t staging_words = 0;
-    int ar_resident[17] = {0};
+    int ar_resident[kArMaxPpt + 1] = {0};
     std::mutex mu;
     uint32_t debug_flags = 0;
     int64_t debug_arg = -1;
@@ -279,7 +279,7 @@ are_status are_workspace_create(are_ws** out, const are_caps* caps) {
         e = cudaMalloc(&ws->d_staging, ws->staging_words * 4);
     }
     if (e == cudaSuccess) {
-        for (int ppt = 1; ppt <= 16; ppt <<= 1) ws->ar_resident[ppt] = ar_rmsnorm_resident_blocks(ppt, ws->num_sms);
+        for (int ppt = 1; ppt <= kArMaxPpt; ++ppt) ws->ar_resident[ppt] = ar_rmsnorm_resident_blocks(ppt, ws->num_sms);
     }
     if (e != cudaSuccess) {
         are_status st = from_cuda(e);
@@ -390,12 +390,13 @@ are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf1
     p.M = (int)M;
     p.N = (int)N;
     p.packs_per_row = (int)(N / 8);
-    int ppt = 1;
-    while (ppt * kArThreads < p.packs_per_row) ppt <<= 1;
-    const int resident = ws->ar_resident[ppt];
+    const int ppt = ar_rmsnorm_ppt(p.packs_per_row);
+    const int resident = ppt > 0 ? ws->ar_resident[ppt] : 0;
     if (resident <= 0) return ARE_ECUDA;
     const int grid = std::min(resident, 2 * ws->num_sms);
     p.chunk_rows = grid;
+    ar_rmsnorm_smem_plan(p);
+    p.ring_slots = (M + grid - 1) / grid > kArRingSlots ? kArRingSlots : 0;
     p.num_chunks = (int)ceil_div(M, grid);
     p.eps = eps;
     p.inv_n = 1.0f / (float)N;

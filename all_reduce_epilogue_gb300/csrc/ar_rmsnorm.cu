@@ -14,22 +14,47 @@
 //     the grid never exceeds the co-resident block count, so the spin cannot
 //     wait on a block that is not running.
 //
-// One-GPU design: the R "ranks" are R device buffers.  Phase A (reduce) and
-// phase B (norm) are decoupled by rows: the rows are cut into chunks of
-// `chunk_rows` (<= grid) rows; in pipeline step `it` every block first stages
-// its share of chunk `it` (a contiguous slice of the chunk's packs), then
-// normalises one row of chunk `it-1`, the row whose packs another block
-// staged (row i of a chunk goes to block (i + grid/2) mod grid).  A chunk is
-// staged one step before it is consumed, so spins are short and the staged
-// fp32 words are read back while they still sit in L2.  The staging words are
-// fp32: staging a bf16 sum would round before the residual add.
+// One-GPU design.  The R "ranks" are R device buffers.  Rows are cut into
+// chunks of `chunk_rows` (= grid) rows.  Each block stages a contiguous slice
+// of every chunk's 8-element packs (phase A) and normalises one row of every
+// chunk (phase B), a row that another block staged: row i of a chunk goes to
+// block (i + grid/2) mod grid.
+//
+// One block per SM, warp-specialised (512 threads):
+//   warp 0      producer: streams, with 1D bulk copies into shared memory,
+//               the R partial slices of every phase-A sub-chunk (224 packs)
+//               into a ring of `stages` buffers, and the residual row of
+//               every phase-B row into a 3-slot ring;
+//   warps 1-7   phase A: each thread sums one pack of the R ranks from shared
+//               memory in ring order, canonicalises, and stores 8 fp32
+//               staging words;
+//   warps 8-15  phase B: bounded spin per 16-byte staging pack, re-arm,
+//               residual add, sum of squares, reduction, scale, store.
+// Phase A runs at most four chunks ahead of this block's phase B.  When the
+// rows wrap, the staging words form a ring of 8 chunk slots (~35 MB at
+// N = 7168) that stays in L2 and is overwritten lap after lap, so staged
+// words are neither written back to nor read from DRAM; the bytes in flight
+// come from the copy engine, not from registers.  The staging words
+// are fp32: staging a bf16 sum would round before the residual add.
 #include <cuda_bf16.h>
 
 #include "are_internal.h"
 #include "ptx.cuh"
 
+
 namespace are {
 namespace {
+
+constexpr int kAThreads = 224;                // phase-A threads = packs per sub-chunk
+constexpr int kBThreads = 256;                // phase-B threads
+constexpr int kRankBytes = kAThreads * 16;    // one rank's slice of a sub-chunk
+constexpr int kStageBytes = kMaxRanks * kRankBytes;  // 28 KB
+constexpr int kResSlots = 3;
+constexpr int kAhead = 4;                     // phase A may lead phase B by this many chunks
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr size_t kTailBytes = 1024;           // barriers, reduction scratch, flags
+
+static_assert(kArThreads == 32 + kAThreads + kBThreads, "warp roles");
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -39,46 +64,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ bool has_sentinel(const uint4& v) {
-    return (v.x == kSentinelF32) | (v.y == kSentinelF32) | (v.z == kSentinelF32) | (v.w == kSentinelF32);
+constexpr uint32_t kSentinelOdd = 0xFFFFFFFFu;  // odd laps of the staging ring
+constexpr uint32_t kCanonicalNaN = 0x7FC00000u;
+
+__device__ __forceinline__ bool has_word(const uint4& v, uint32_t s) {
+    return (v.x == s) | (v.y == s) | (v.z == s) | (v.w == s);
+}
+__device__ __forceinline__ bool all_words(const uint4& v, uint32_t s) {
+    return (v.x == s) & (v.y == s) & (v.z == s) & (v.w == s);
 }
 
 __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
     f[0] = bf_lo(v.x); f[1] = bf_hi(v.x); f[2] = bf_lo(v.y); f[3] = bf_hi(v.y);
     f[4] = bf_lo(v.z); f[5] = bf_hi(v.z); f[6] = bf_lo(v.w); f[7] = bf_hi(v.w);
-}
-
-// Phase A for one 8-element pack: ring-order fp32 sum of the R bf16 values,
-// -0.0 -> +0.0, two 16-byte stores into the staging words.
-__device__ __forceinline__ void stage_pack(const ArParams& p, int64_t e, int64_t pack_id, uint32_t& ncanon) {
-    uint4 v[kMaxRanks];
-#pragma unroll
-    for (int r = 0; r < kMaxRanks; ++r)
-        if (r < p.R) v[r] = ptx::ld_stream_v4(p.x[r] + e);
-    float acc[8];
-    unpack8(v[0], acc);
-#pragma unroll
-    for (int r = 1; r < kMaxRanks; ++r) {
-        if (r < p.R) {
-            float f[8];
-            unpack8(v[r], f);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = acc[i] + f[i];
-        }
-    }
-    uint32_t w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        w[i] = __float_as_uint(acc[i]);
-        if (w[i] == kSentinelF32) {  // producer-side canonicalisation
-            w[i] = 0u;
-            ++ncanon;
-        }
-    }
-    if ((p.flags & ARE_DEBUG_SKIP_STAGE) && pack_id == p.debug_arg) return;
-    uint32_t* dst = p.staging + e;
-    ptx::st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
-    ptx::st_v4(dst + 4, make_uint4(w[4], w[5], w[6], w[7]));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -87,33 +85,141 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Phase B for one row: bounded spin on the staged packs, re-arm, residual add,
-// sum of squares, block reduction, scale by rsqrt(ms + eps) * gamma, store.
+__device__ __forceinline__ void b_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kBThreads) : "memory"); }
+
+struct Shared {
+    uint8_t* stage;     // stages x 28 KB
+    uint8_t* res;       // kResSlots x N*2 bytes (when the residual is staged in shared memory)
+    uint64_t* full;     // [stages]
+    uint64_t* empty;    // [stages]
+    uint64_t* rfull;    // [kResSlots]
+    uint64_t* rempty;   // [kResSlots]
+    float* red;         // [16]
+    volatile int* bdone;        // chunks phase B has finished
+    volatile uint32_t* abort;   // block gave up
+};
+
+__device__ __forceinline__ Shared carve(uint8_t* base, const ArParams& p) {
+    Shared s;
+    s.stage = base;
+    s.res = base + (size_t)p.stages * kStageBytes;
+    uint8_t* tail = s.res + (p.res_in_smem ? (size_t)kResSlots * p.N * 2 : 0);
+    tail = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tail) + 15) & ~uintptr_t(15));
+    s.full = reinterpret_cast<uint64_t*>(tail);
+    s.empty = s.full + kMaxArStages;
+    s.rfull = s.empty + kMaxArStages;
+    s.rempty = s.rfull + kResSlots;
+    s.red = reinterpret_cast<float*>(s.rempty + kResSlots);
+    s.bdone = reinterpret_cast<volatile int*>(s.red + 16);
+    s.abort = reinterpret_cast<volatile uint32_t*>(s.bdone + 1);
+    return s;
+}
+
+// Bounded wait on a shared-memory barrier phase; false once the block gave up.
+__device__ __forceinline__ bool ar_wait(uint64_t* bar, uint32_t parity, const Shared& sh, const ArParams& p) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*sh.abort) return false;
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            record_error(p.status, ARE_DEV_PIPE_TIMEOUT, blockIdx.x, -1, -1);
+            *sh.abort = 1u;
+            return false;
+        }
+    }
+}
+
+// Rows of chunk c, and this block's slice [q0, q1) of its packs (chunk-local
+// pack indices; the chunk's first pack is `base`).
+struct Slice {
+    int64_t base, q0, q1;
+    int rows;
+};
+// Without a ring the chunk's packs are split evenly over the blocks.  With a
+// ring every block stages exactly row blockIdx.x of every chunk (chunk_rows ==
+// grid), so each staging position has the same producer in every lap: its own
+// earlier write of the position then orders its check of the next lap's
+// sentinel, however far the blocks drift apart.
+__device__ __forceinline__ Slice slice_of(const ArParams& p, int c) {
+    const int64_t row0 = (int64_t)c * p.chunk_rows;
+    Slice s;
+    s.rows = (int)min((int64_t)p.chunk_rows, (int64_t)p.M - row0);
+    s.base = row0 * p.packs_per_row;
+    if (p.ring_slots) {
+        const int64_t r = blockIdx.x < s.rows ? blockIdx.x : s.rows;
+        s.q0 = r * p.packs_per_row;
+        s.q1 = blockIdx.x < s.rows ? s.q0 + p.packs_per_row : s.q0;
+        return s;
+    }
+    const int64_t total = (int64_t)s.rows * p.packs_per_row;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    s.q0 = min(total, (int64_t)blockIdx.x * per);
+    s.q1 = min(total, s.q0 + per);
+    return s;
+}
+
+// First staging word of row i of chunk c: the rows of chunk c live at
+// c*chunk_rows, or in ring slot c mod ring_slots when the rows wrap.
+__device__ __forceinline__ uint32_t* staging_row(const ArParams& p, int c, int64_t i) {
+    const int64_t r0 = p.ring_slots ? (int64_t)(c % p.ring_slots) * p.chunk_rows : (int64_t)c * p.chunk_rows;
+    return p.staging + (r0 + i) * (int64_t)p.N;
+}
+
+// Ring mode (rows wrap over `ring_slots` staging slots).  Lap L of slot s is
+// chunk s + L*ring_slots.  Between laps the slot's words hold the sentinel of
+// the next lap: -0.0 for even laps, 0xFFFFFFFF (a NaN pattern that staged data
+// never has: NaNs are canonicalised like -0.0) for odd laps; the last lap of
+// every slot re-arms with -0.0, so between calls every word is -0.0 again.
+//  * A consumer position is served by the same thread in every lap, so its own
+//    re-arm precedes (in program order) its next read of that position.
+//  * A producer overwrites a pack only after reading the lap's sentinel in
+//    all of its words: its write is then ordered after the consumer's re-arm.
+//    Each position also has a fixed producer (see slice_of), which wrote the
+//    position two laps earlier itself, so the sentinel it reads cannot be the
+//    same-parity one from before that write.
+// No counter, fence or barrier couples the blocks.
+__device__ __forceinline__ int lap_of(const ArParams& p, int c) { return p.ring_slots ? c / p.ring_slots : 0; }
+__device__ __forceinline__ uint32_t sentinel_of(int lap) { return (lap & 1) ? kSentinelOdd : kSentinelF32; }
+// Value a consumer writes back into row i of chunk c: the next lap's sentinel
+// if a later chunk of this call stages that row of the slot, else -0.0.
+__device__ __forceinline__ uint32_t rearm_value(const ArParams& p, int c, int i) {
+    if (!p.ring_slots || c + p.ring_slots >= p.num_chunks) return kSentinelF32;
+    const int64_t next_rows = min((int64_t)p.chunk_rows, (int64_t)p.M - (int64_t)(c + p.ring_slots) * p.chunk_rows);
+    if (i >= next_rows) return kSentinelF32;
+    return sentinel_of(c / p.ring_slots + 1);
+}
+
+__device__ __forceinline__ int consumed_row(int G) {
+    int i = (int)blockIdx.x - G / 2;
+    return i < 0 ? i + G : i;
+}
+
+// ------------------------------------------------------------------ phase B
 template <int PPT>
-__device__ __forceinline__ void norm_row(const ArParams& p, int64_t row, float* red) {
-    const int tid = threadIdx.x;
+__device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, int64_t row, uint32_t* srow, int bt,
+                                         const uint8_t* res_smem, uint64_t keep, uint32_t sent, uint32_t rearm) {
     const int P = p.packs_per_row;
-    uint32_t* srow = p.staging + row * (int64_t)p.N;
     uint4 lo[PPT], hi[PPT], res[PPT];
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-        const int pk = tid + k * kArThreads;
+        const int pk = bt + k * kBThreads;
         if (pk < P) {
             lo[k] = ptx::ld_relaxed_gpu_v4(srow + pk * 8);
             hi[k] = ptx::ld_relaxed_gpu_v4(srow + pk * 8 + 4);
-            if (p.residual) res[k] = ptx::ld_stream_v4(p.residual + row * (int64_t)p.N + pk * 8);
+            if (p.residual && !res_smem) res[k] = ptx::ld_stream_v4(p.residual + row * (int64_t)p.N + pk * 8);
         }
     }
     bool ok = true;
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-        const int pk = tid + k * kArThreads;
-        if (pk < P && (has_sentinel(lo[k]) || has_sentinel(hi[k]))) {
+        const int pk = bt + k * kBThreads;
+        if (pk < P && (has_word(lo[k], sent) || has_word(hi[k], sent))) {
             const uint64_t t0 = ptx::globaltimer();
             while (true) {
                 lo[k] = ptx::ld_relaxed_gpu_v4(srow + pk * 8);
                 hi[k] = ptx::ld_relaxed_gpu_v4(srow + pk * 8 + 4);
-                if (!has_sentinel(lo[k]) && !has_sentinel(hi[k])) break;
+                if (!has_word(lo[k], sent) && !has_word(hi[k], sent)) break;
                 if (ptx::ld_relaxed_gpu(&p.status->code) != 0u) { ok = false; break; }
                 if (ptx::globaltimer() - t0 > p.timeout_ns) {
                     record_error(p.status, ARE_DEV_STAGE_TIMEOUT, blockIdx.x, (int32_t)row, pk);
@@ -125,21 +231,28 @@ __device__ __forceinline__ void norm_row(const ArParams& p, int64_t row, float* 
     }
     // Re-arm every pack this thread consumed (it is the pack's only consumer).
     if (ok && !(p.flags & ARE_DEBUG_NO_REARM)) {
-        const uint4 s = make_uint4(kSentinelF32, kSentinelF32, kSentinelF32, kSentinelF32);
+        const uint4 s = make_uint4(rearm, rearm, rearm, rearm);
 #pragma unroll
         for (int k = 0; k < PPT; ++k) {
-            const int pk = tid + k * kArThreads;
+            const int pk = bt + k * kBThreads;
             if (pk < P) {
-                ptx::st_v4(srow + pk * 8, s);
-                ptx::st_v4(srow + pk * 8 + 4, s);
+                ptx::st_v4_hint(srow + pk * 8, s, keep);
+                ptx::st_v4_hint(srow + pk * 8 + 4, s, keep);
             }
+        }
+    }
+    if (p.residual && res_smem) {
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            const int pk = bt + k * kBThreads;
+            if (pk < P) res[k] = *reinterpret_cast<const uint4*>(res_smem + pk * 16);
         }
     }
     // h = s + residual, kept in place in the staged registers
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-        const int pk = tid + k * kArThreads;
+        const int pk = bt + k * kBThreads;
         if (pk < P) {
             float f[8] = {__uint_as_float(lo[k].x), __uint_as_float(lo[k].y), __uint_as_float(lo[k].z),
                           __uint_as_float(lo[k].w), __uint_as_float(hi[k].x), __uint_as_float(hi[k].y),
@@ -158,20 +271,20 @@ __device__ __forceinline__ void norm_row(const ArParams& p, int64_t row, float* 
                                __float_as_uint(f[7]));
         }
     }
-    const int warp = tid >> 5, lane = tid & 31;
+    const int w = bt >> 5, lane = bt & 31;
     ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    __syncthreads();
-    if (warp == 0) {
-        float v = lane < (kArThreads / 32) ? red[lane] : 0.f;
+    if (lane == 0) sh.red[w] = ss;
+    b_bar();
+    if (w == 0) {
+        float v = lane < (kBThreads / 32) ? sh.red[lane] : 0.f;
         v = warp_sum(v);
-        if (lane == 0) red[kArThreads / 32] = v;
+        if (lane == 0) sh.red[kBThreads / 32] = v;
     }
-    __syncthreads();
-    const float inv = rsqrtf(red[kArThreads / 32] * p.inv_n + p.eps);
+    b_bar();
+    const float inv = rsqrtf(sh.red[kBThreads / 32] * p.inv_n + p.eps);
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-        const int pk = tid + k * kArThreads;
+        const int pk = bt + k * kBThreads;
         if (pk < P) {
             const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
             const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
@@ -185,47 +298,191 @@ __device__ __forceinline__ void norm_row(const ArParams& p, int64_t row, float* 
     }
 }
 
-// Blocks per SM the register budget is tuned for (the grid is still clamped
-// by the runtime's occupancy query).
 template <int PPT>
-struct ArMinBlocks {
-    static constexpr int value = PPT <= 8 ? 2 : 1;
-};
-
-template <int PPT>
-__global__ void __launch_bounds__(kArThreads, ArMinBlocks<PPT>::value) ar_rmsnorm_kernel(const __grid_constant__ ArParams p) {
-    __shared__ float red[kArThreads / 32 + 1];
+__global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_constant__ ArParams p) {
+    extern __shared__ __align__(128) uint8_t ar_smem[];
+    const Shared sh = carve(ar_smem, p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
-    const int b = blockIdx.x;
-    const int P = p.packs_per_row;
-    int consume = b - G / 2;  // chunk-local row this block normalises
-    if (consume < 0) consume += G;
-    uint32_t ncanon = 0;
+    const int consume = consumed_row(G);
+    const bool res_smem = p.residual != nullptr && p.res_in_smem;
 
-    for (int it = 0; it <= p.num_chunks; ++it) {
-        if (it < p.num_chunks) {  // phase A: stage chunk `it`
-            const int64_t row0 = (int64_t)it * p.chunk_rows;
-            const int rows = min((int64_t)p.chunk_rows, (int64_t)p.M - row0);
-            const int64_t total = (int64_t)rows * P;
-            const int64_t per = (total + G - 1) / G;
-            const int64_t q0 = (int64_t)b * per;
-            const int64_t q1 = min(total, q0 + per);
-            for (int64_t q = q0 + threadIdx.x; q < q1; q += kArThreads) {
-                const int64_t qa = row0 * P + q;
-                stage_pack(p, qa * 8, qa, ncanon);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            ptx::mbar_init(&sh.full[s], 1);
+            ptx::mbar_init(&sh.empty[s], kAThreads);
+        }
+        for (int s = 0; s < kResSlots; ++s) {
+            ptx::mbar_init(&sh.rfull[s], 1);
+            ptx::mbar_init(&sh.rempty[s], kBThreads);
+        }
+        *sh.bdone = 0;
+        *sh.abort = 0u;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_shared();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t stream_pol = ptx::policy_evict_first();
+            int s = 0, rs = 0;
+            uint32_t ph = 0, rph = 0;
+            uint32_t issued = 0, issued_ph = 0, rissued = 0, rissued_ph = 0;
+            bool ok = true;
+            for (int c = 0; c < p.num_chunks && ok; ++c) {
+                const Slice sl = slice_of(p, c);
+                if (res_smem && consume < sl.rows) {  // residual row of this block's phase-B row
+                    if (!ar_wait(&sh.rempty[rs], rph ^ 1u, sh, p)) break;
+                    const uint32_t bytes = (uint32_t)p.N * 2;
+                    ptx::mbar_arrive_expect_tx(&sh.rfull[rs], bytes);
+                    const int64_t row = (int64_t)c * p.chunk_rows + consume;
+                    ptx::bulk_load_hint(sh.res + (size_t)rs * p.N * 2, p.residual + row * (int64_t)p.N, bytes,
+                                        &sh.rfull[rs], stream_pol);
+                    rissued |= 1u << rs;
+                    rissued_ph = (rissued_ph & ~(1u << rs)) | (rph << rs);
+                    if (++rs == kResSlots) { rs = 0; rph ^= 1u; }
+                }
+                for (int64_t q = sl.q0; q < sl.q1; q += kAThreads) {
+                    const int n = (int)min((int64_t)kAThreads, sl.q1 - q);
+                    if (!ar_wait(&sh.empty[s], ph ^ 1u, sh, p)) { ok = false; break; }
+                    ptx::mbar_arrive_expect_tx(&sh.full[s], (uint32_t)(p.R * n * 16));
+                    for (int r = 0; r < p.R; ++r)
+                        ptx::bulk_load_hint(sh.stage + (size_t)s * kStageBytes + r * kRankBytes,
+                                            p.x[r] + (sl.base + q) * 8, (uint32_t)(n * 16), &sh.full[s], stream_pol);
+                    issued |= 1u << s;
+                    issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+                    if (++s == p.stages) { s = 0; ph ^= 1u; }
+                }
+            }
+            // every bulk copy issued must land before the block exits
+            for (int i = 0; i < p.stages; ++i) {
+                if (issued & (1u << i)) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (!ptx::mbar_try_wait(&sh.full[i], (issued_ph >> i) & 1u))
+                        if (ptx::globaltimer() - t0 > p.timeout_ns) break;
+                }
+            }
+            for (int i = 0; i < kResSlots; ++i) {
+                if (rissued & (1u << i)) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (!ptx::mbar_try_wait(&sh.rfull[i], (rissued_ph >> i) & 1u))
+                        if (ptx::globaltimer() - t0 > p.timeout_ns) break;
+                }
             }
         }
-        if (it >= 1) {  // phase B: normalise one row of chunk `it - 1`
-            const int64_t row0 = (int64_t)(it - 1) * p.chunk_rows;
-            const int rows = min((int64_t)p.chunk_rows, (int64_t)p.M - row0);
-            if (consume < rows) norm_row<PPT>(p, row0 + consume, red);
-        }
-    }
-    if (p.flags & ARE_DEBUG_COUNT_CANON) {
-        uint32_t c = ncanon;
+    } else if (warp < 8) {
+        // ---------------------------------------------------------------- phase A
+        const int at = threadIdx.x - 32;
+        const uint64_t keep = ptx::policy_evict_last();
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t ncanon = 0;
+        for (int c = 0; c < p.num_chunks; ++c) {
+            if (c >= kAhead) {  // stay at most kAhead chunks ahead of this block's phase B
+                const uint64_t t0 = ptx::globaltimer();
+                while (*sh.bdone < c - kAhead + 1) {
+                    if (*sh.abort) break;
+                    if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                        record_error(p.status, ARE_DEV_PIPE_TIMEOUT, blockIdx.x, -2, c);
+                        *sh.abort = 1u;
+                        break;
+                    }
+                }
+            }
+            const Slice sl = slice_of(p, c);
+            uint32_t* chunk_staging = staging_row(p, c, 0);
+            const int lap = lap_of(p, c);
+            const uint32_t sent = sentinel_of(lap);
+            for (int64_t q = sl.q0; q < sl.q1; q += kAThreads) {
+                const int n = (int)min((int64_t)kAThreads, sl.q1 - q);
+                uint32_t* dst = chunk_staging + (q + at) * 8;
+                // ring laps >= 1: read the target pack (its consumer's re-arm) before overwriting it;
+                // issued before the wait for the partials so the two latencies overlap
+                uint4 chk0 = make_uint4(sent, sent, sent, sent), chk1 = chk0;
+                if (lap > 0 && at < n) {
+                    chk0 = ptx::ld_relaxed_gpu_v4(dst);
+                    chk1 = ptx::ld_relaxed_gpu_v4(dst + 4);
+                }
+                const bool ready = ar_wait(&sh.full[s], ph, sh, p);
+                if (lap > 0 && at < n && !(all_words(chk0, sent) && all_words(chk1, sent))) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (true) {
+                        chk0 = ptx::ld_relaxed_gpu_v4(dst);
+                        chk1 = ptx::ld_relaxed_gpu_v4(dst + 4);
+                        if (all_words(chk0, sent) && all_words(chk1, sent)) break;
+                        if (*sh.abort || ptx::ld_relaxed_gpu(&p.status->code) != 0u) break;
+                        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                            record_error(p.status, ARE_DEV_PIPE_TIMEOUT, blockIdx.x, -3, c);
+                            *sh.abort = 1u;
+                            break;
+                        }
+                    }
+                }
+                if (ready && at < n) {
+                    const uint8_t* src = sh.stage + (size_t)s * kStageBytes + at * 16;
+                    float acc[8];
+                    unpack8(*reinterpret_cast<const uint4*>(src), acc);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
-        if ((threadIdx.x & 31) == 0 && c) atomicAdd(&p.counters[0], (unsigned long long)c);
+                    for (int r = 1; r < kMaxRanks; ++r) {
+                        if (r < p.R) {
+                            float f[8];
+                            unpack8(*reinterpret_cast<const uint4*>(src + r * kRankBytes), f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) acc[i] = acc[i] + f[i];
+                        }
+                    }
+                    uint32_t wv[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        wv[i] = __float_as_uint(acc[i]);
+                        if (wv[i] == kSentinelF32) {  // producer-side canonicalisation
+                            wv[i] = 0u;
+                            ++ncanon;
+                        }
+                        if (acc[i] != acc[i]) wv[i] = kCanonicalNaN;  // never a ring sentinel
+                    }
+                    const int64_t pack = sl.base + q + at;
+                    if (!((p.flags & ARE_DEBUG_SKIP_STAGE) && pack == p.debug_arg)) {
+                        ptx::st_v4_hint(dst, make_uint4(wv[0], wv[1], wv[2], wv[3]), keep);
+                        ptx::st_v4_hint(dst + 4, make_uint4(wv[4], wv[5], wv[6], wv[7]), keep);
+                    }
+                }
+                ptx::mbar_arrive(&sh.empty[s]);
+                if (++s == p.stages) { s = 0; ph ^= 1u; }
+            }
+        }
+        if (p.flags & ARE_DEBUG_COUNT_CANON) {
+            uint32_t cnt = ncanon;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xFFFFFFFFu, cnt, o);
+            if (lane == 0 && cnt) atomicAdd(&p.counters[0], (unsigned long long)cnt);
+        }
+    } else {
+        // ---------------------------------------------------------------- phase B
+        const int bt = threadIdx.x - 256;
+        const uint64_t keep = ptx::policy_evict_last();
+        int rs = 0;
+        uint32_t rph = 0;
+        for (int c = 0; c < p.num_chunks; ++c) {
+            const int64_t row0 = (int64_t)c * p.chunk_rows;
+            const int rows = (int)min((int64_t)p.chunk_rows, (int64_t)p.M - row0);
+            if (consume < rows) {
+                const uint8_t* res_src = nullptr;
+                if (res_smem) {
+                    ar_wait(&sh.rfull[rs], rph, sh, p);
+                    res_src = sh.res + (size_t)rs * p.N * 2;
+                }
+                norm_row<PPT>(p, sh, row0 + consume, staging_row(p, c, consume), bt, res_src, keep,
+                              sentinel_of(lap_of(p, c)), rearm_value(p, c, consume));
+                if (res_smem) {
+                    ptx::mbar_arrive(&sh.rempty[rs]);
+                    if (++rs == kResSlots) { rs = 0; rph ^= 1u; }
+                }
+            }
+            if (bt == 0) *sh.bdone = c + 1;
+        }
     }
 }
 
@@ -236,13 +493,38 @@ __global__ void fill_u32_kernel(uint32_t* dst, uint32_t v, size_t n) {
 
 template <int PPT>
 int resident(int num_sms) {
+    if (cudaFuncSetAttribute(ar_rmsnorm_kernel<PPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemLimit) != cudaSuccess)
+        return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ar_rmsnorm_kernel<PPT>, kArThreads, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ar_rmsnorm_kernel<PPT>, kArThreads, kSmemLimit) !=
+        cudaSuccess)
         return 0;
     return n * num_sms;
 }
 
 }  // namespace
+
+int ar_rmsnorm_ppt(int packs_per_row) {
+    static const int kPpts[] = {1, 2, 4, 8, 16};
+    for (int v : kPpts)
+        if (v * kBThreads >= packs_per_row) return v;
+    return 0;
+}
+
+void ar_rmsnorm_smem_plan(ArParams& p) {
+    // residual rows in shared memory when three of them leave room for >= 4 stages
+    const size_t res_bytes = (size_t)kResSlots * p.N * 2;
+    p.res_in_smem = (p.residual != nullptr && res_bytes + 4 * (size_t)kStageBytes + kTailBytes <= kSmemLimit) ? 1 : 0;
+    const size_t avail = kSmemLimit - kTailBytes - (p.res_in_smem ? res_bytes : 0);
+    int st = (int)(avail / kStageBytes);
+    if (st > kMaxArStages) st = kMaxArStages;
+    p.stages = st;
+}
+
+size_t ar_rmsnorm_smem_bytes(const ArParams& p) {
+    return (size_t)p.stages * kStageBytes + (p.res_in_smem ? (size_t)kResSlots * p.N * 2 : 0) + kTailBytes;
+}
 
 int ar_rmsnorm_resident_blocks(int ppt, int num_sms) {
     switch (ppt) {
@@ -256,12 +538,13 @@ int ar_rmsnorm_resident_blocks(int ppt, int num_sms) {
 }
 
 cudaError_t launch_ar_rmsnorm(const ArParams& p, int ppt, int grid, cudaStream_t stream) {
+    const size_t smem = ar_rmsnorm_smem_bytes(p);
     switch (ppt) {
-        case 1: ar_rmsnorm_kernel<1><<<grid, kArThreads, 0, stream>>>(p); break;
-        case 2: ar_rmsnorm_kernel<2><<<grid, kArThreads, 0, stream>>>(p); break;
-        case 4: ar_rmsnorm_kernel<4><<<grid, kArThreads, 0, stream>>>(p); break;
-        case 8: ar_rmsnorm_kernel<8><<<grid, kArThreads, 0, stream>>>(p); break;
-        case 16: ar_rmsnorm_kernel<16><<<grid, kArThreads, 0, stream>>>(p); break;
+        case 1: ar_rmsnorm_kernel<1><<<grid, kArThreads, smem, stream>>>(p); break;
+        case 2: ar_rmsnorm_kernel<2><<<grid, kArThreads, smem, stream>>>(p); break;
+        case 4: ar_rmsnorm_kernel<4><<<grid, kArThreads, smem, stream>>>(p); break;
+        case 8: ar_rmsnorm_kernel<8><<<grid, kArThreads, smem, stream>>>(p); break;
+        case 16: ar_rmsnorm_kernel<16><<<grid, kArThreads, smem, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

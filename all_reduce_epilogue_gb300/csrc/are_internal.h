@@ -29,14 +29,16 @@ __device__ __forceinline__ void record_error(DevStatus* st, uint32_t code, uint3
 
 // ------------------------------------------------------------------ AR+RMSNorm
 constexpr uint32_t kSentinelF32 = 0x80000000u;  // -0.0 as an fp32 word
-constexpr int kArThreads = 256;
+constexpr int kArThreads = 512;   // 1 producer warp + 7 phase-A warps + 8 phase-B warps
+constexpr int kMaxArStages = 8;   // phase-A shared-memory stages (upper bound)
+constexpr int kArRingSlots = 8;   // staging ring slots (chunks) when the rows wrap
 
 struct ArParams {
     const uint16_t* x[kMaxRanks];  // R bf16 partials [M, N]
     const uint16_t* residual;      // bf16 [M, N] or nullptr
     const float* gamma;            // fp32 [N]
     uint16_t* out;                 // bf16 [M, N]
-    uint32_t* staging;             // fp32 words [M, N], armed with the sentinel
+    uint32_t* staging;             // fp32 words, armed with the sentinel (chunk rows, see ring_slots)
     DevStatus* status;
     unsigned long long* counters;  // debug counters
     int R;
@@ -45,6 +47,9 @@ struct ArParams {
     int packs_per_row;  // N / 8
     int chunk_rows;     // rows per pipeline chunk (<= grid)
     int num_chunks;
+    int ring_slots;     // 0: chunk c's rows at c*chunk_rows; else staging slot c % ring_slots
+    int stages;         // phase-A shared-memory stages (set by ar_rmsnorm_smem_plan)
+    int res_in_smem;    // residual rows streamed into shared memory (set by ar_rmsnorm_smem_plan)
     float eps;
     float inv_n;
     uint32_t flags;
@@ -52,6 +57,12 @@ struct ArParams {
     uint64_t timeout_ns;
 };
 
+// Packs-per-thread variant for a row of `packs_per_row` 8-element packs (0 if too wide).
+int ar_rmsnorm_ppt(int packs_per_row);
+constexpr int kArMaxPpt = 20;
+// Choose the phase-A stage count and whether residual rows go through shared
+// memory (needs p.N and p.residual set).
+void ar_rmsnorm_smem_plan(ArParams& p);
 // Largest grid that is fully co-resident for the packs-per-thread variant `ppt`.
 int ar_rmsnorm_resident_blocks(int ppt, int num_sms);
 cudaError_t launch_ar_rmsnorm(const ArParams& p, int ppt, int grid, cudaStream_t stream);

@@ -34,7 +34,7 @@ static __device__ __align__(256) uint32_t g_noalloc_scratch[kHeaderWords + kStag
 struct DeviceScratch {
     uint32_t* base = nullptr;  // device address of g_noalloc_scratch on this device
     int num_sms = 0;
-    int resident[17] = {0};
+    int resident[kArMaxPpt + 1] = {0};
 };
 
 std::mutex g_mu;
@@ -57,7 +57,7 @@ are_status setup_current_device(DeviceScratch** out) {
         void* ptr = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || ptr == nullptr) return ARE_ECUDA;
-        for (int ppt = 1; ppt <= 16; ppt <<= 1) d.resident[ppt] = ar_rmsnorm_resident_blocks(ppt, sms);
+        for (int ppt = 1; ppt <= kArMaxPpt; ++ppt) d.resident[ppt] = ar_rmsnorm_resident_blocks(ppt, sms);
         d.num_sms = sms;
         d.base = static_cast<uint32_t*>(ptr);
     }
@@ -102,12 +102,13 @@ extern "C" are_status are_allreduce_rmsnorm_noalloc(const are_bf16* const partia
     p.M = (int)M;
     p.N = (int)N;
     p.packs_per_row = (int)(N / 8);
-    int ppt = 1;
-    while (ppt * kArThreads < p.packs_per_row) ppt <<= 1;
-    const int resident = d->resident[ppt];
+    const int ppt = ar_rmsnorm_ppt(p.packs_per_row);
+    const int resident = ppt > 0 ? d->resident[ppt] : 0;
     if (resident <= 0) return ARE_ECUDA;
     const int grid = resident < 2 * d->num_sms ? resident : 2 * d->num_sms;
     p.chunk_rows = grid;
+    ar_rmsnorm_smem_plan(p);
+    p.ring_slots = (M + grid - 1) / grid > kArRingSlots ? kArRingSlots : 0;
     p.num_chunks = (int)((M + grid - 1) / grid);
     p.eps = eps;
     p.inv_n = 1.0f / (float)N;

@@ -46,7 +46,8 @@ def test_workload_shapes(ws, oracle, M):
     got = run(ws, parts, res, gamma)
     ref = oracle.allreduce_rmsnorm(parts, res, gamma, 1e-6)
     oracle_mod_check(got, ref, f"M={M}")
-    # every staged word consumed and re-armed
+    # every staged word consumed and re-armed with -0.0 (the ring's odd-lap
+    # sentinel never survives a call)
     assert np.all(staging_words(ws, M, 7168) == SENT)
 
 
@@ -110,7 +111,7 @@ def test_repeat_rearm(ws, oracle):
     import all_reduce_epilogue_gb300 as are
     N = 7168
     cases = []
-    for i, M in enumerate([64, 1, 513, 8, 300]):
+    for i, M in enumerate([64, 1, 2000, 513, 8, 300, 4096]):
         parts, res, gamma = synth.ar_inputs(8, M, N, 500 + i)
         cases.append(([dev_bf16(x) for x in parts], dev_bf16(res), torch.from_numpy(gamma).cuda(),
                       torch.empty((M, N), dtype=torch.bfloat16, device="cuda"),
@@ -122,7 +123,7 @@ def test_repeat_rearm(ws, oracle):
     assert st["code"] == 0, st
     for p, r, g, out, ref in cases:
         check_close(host_f32(out), ref, "repeat")
-    assert np.all(staging_words(ws, 1024, N) == SENT)
+    assert np.all(staging_words(ws, 4096, N) == SENT)
 
 
 def test_missing_pack_times_out_and_reset_recovers(oracle):
@@ -168,3 +169,29 @@ def test_bad_arguments(ws):
     assert e.value.status == are.ECAPACITY
     empty = torch.zeros((0, 64), dtype=torch.bfloat16, device="cuda")
     are.allreduce_rmsnorm([empty], None, g, 1e-6, torch.empty_like(empty), ws)  # M = 0: no-op
+
+
+@pytest.mark.parametrize("M", [8192, 7000])
+def test_ring_many_laps_repeat(oracle, M):
+    """Many laps of the staging ring with a partial last chunk, called
+    repeatedly: every staging position must be overwritten only after its
+    consumer re-armed it (a producer running laps ahead would corrupt or
+    stall a later lap)."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    N = 7168
+    parts, res, gamma = synth.ar_inputs(8, M, N, 77 + M)
+    ref = oracle.allreduce_rmsnorm(parts, res, gamma, 1e-6)
+    P = [dev_bf16(x) for x in parts]
+    r = dev_bf16(res)
+    g = torch.from_numpy(gamma).cuda()
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with are.Workspace(R_max=8, M_max=M, N_max=N, timeout_ns=100_000_000) as w:
+        for _ in range(30):
+            are.allreduce_rmsnorm(P, r, g, 1e-6, out, w)
+        st = w.device_status()
+        assert st["code"] == 0, st
+        check_close(host_f32(out), ref, f"ring M={M}")
+        assert np.all(staging_words(w, M, N) == SENT)
