@@ -191,12 +191,23 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     p->num_tiles = (int)T;
     p->num_units = (int)(T * R);
     p->num_kb = (int)ceil_div(K, kBK);
-    p->group_m = (int)std::min<int64_t>(tiles_m, 8);
+    p->pairs_m = (int)((tiles_m + 1) / 2);
+    p->num_pair_units = (int)(p->pairs_m * tiles_n * R);
     p->flags = ws->debug_flags;
     p->debug_arg = ws->debug_arg;
     p->timeout_ns = ws->timeout_ns;
-    const int grid = (int)std::min<int64_t>(p->num_units, ws->num_sms);
-    e = launch_gemm_reduce(*p, mode, grid, s);
+    // CTA pairs (256-row tiles) wherever there are at least two tile rows and
+    // the device can co-schedule the clusters; one CTA per tile otherwise.
+    const int clusters = gemm_pair_max_clusters();
+    if (tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA)) {
+        p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
+        const int grid = 2 * (int)std::min<int64_t>(p->num_pair_units, clusters);
+        e = launch_gemm_pair(*p, mode, grid, s);
+    } else {
+        p->group_m = (int)std::min<int64_t>(tiles_m, 8);
+        const int grid = (int)std::min<int64_t>(p->num_units, ws->num_sms);
+        e = launch_gemm_reduce(*p, mode, grid, s);
+    }
     delete p;
     return from_cuda(e);
 }

@@ -85,7 +85,10 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ void b_bar() { asm volatile("bar.sync 2, %0;" ::"n"(kBThreads) : "memory"); }
+__device__ __forceinline__ void b_bar() {
+    __syncwarp();  // .aligned barrier: reconverge the warp first
+    asm volatile("bar.sync 2, %0;" ::"n"(kBThreads) : "memory");
+}
 
 struct Shared {
     uint8_t* stage;     // stages x 28 KB

@@ -96,7 +96,8 @@ struct GemmParams {
     int H;               // output box height (RS)
     int nviews;          // distinct output views (AR)
     int tiles_m, tiles_n, num_tiles, num_units, num_kb;
-    int group_m;         // tile raster: rows of tiles per group
+    int pairs_m, num_pair_units;  // CTA-pair kernel: 256-row tile pairs, R units per pair
+    int group_m;         // tile raster: rows of tiles (pairs) per group
     uint32_t flags;
     int64_t debug_arg;
     uint64_t timeout_ns;
@@ -108,5 +109,9 @@ cudaError_t gemm_prepare_kernels();
 cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                            uint32_t box_outer);
 cudaError_t launch_gemm_reduce(const GemmParams& p, int mode, int grid, cudaStream_t stream);
+// CTA-pair variant (cta_group::2 UMMA, 256x256 per pair); grid = 2 x clusters.
+cudaError_t launch_gemm_pair(const GemmParams& p, int mode, int grid, cudaStream_t stream);
+// Largest number of co-resident 2-CTA clusters of the pair kernel (0 if unavailable).
+int gemm_pair_max_clusters();
 
 }  // namespace are

@@ -116,9 +116,17 @@ __device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, const Gem
     }
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barriers are .aligned: every lane of a warp must arrive together, so
+// each helper first reconverges the warp (lanes that ran a single-lane branch,
+// such as issuing a store or an arrive, would otherwise arrive late and be
+// counted in the barrier's next phase).
+__device__ __forceinline__ void epi_bar() {
+    __syncwarp();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 // Epilogue-wide OR of a predicate (uniform result for all 128 threads).
 __device__ __forceinline__ bool epi_bar_or(bool v) {
+    __syncwarp();
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
@@ -191,6 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
     if (warp == 0 && lane == 0) {
         for (int r = 0; r < p.R; ++r) { ptx::prefetch_tmap(&p.tmA[r]); ptx::prefetch_tmap(&p.tmB[r]); }
     }
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -511,12 +520,473 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
         if (lead && lane < 2) ptx::bulk_wait0();
     }
 
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     if (warp == 2) {
         __syncwarp();
         ptx::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ============================================================================
+// CTA-pair variant: tcgen05.mma.cta_group::2 computes a 256x256 tile per CTA
+// pair (cluster of 2).  Each CTA stages its own 128 rows of A and its own 128
+// columns of B (32 KB per k-block, 4 stages) and holds its 128x256 half of the
+// accumulator in its own TMEM; the leader (cluster rank 0) issues the MMAs.
+// Each CTA's half is one 128x256 output tile with its own mask word and
+// partial slot; the pair computes the same rank r for both halves, and the
+// pair's reducer rank (owner of the pair's first row for GEMM+RS, pair index
+// mod R for GEMM+AR) reduces both halves.
+//
+// The epilogue is split so that no reduction ever holds TMEM:
+//   warps 4-7   drain: TMEM -> registers -> swizzled staging -> 16 KB bulk
+//               stores into the unit's partial slot (fp32 for RS, bf16 for
+//               AR; the reducer's own partial too); the accumulator goes back
+//               to the MMA as soon as it is read, and the unit's bit is
+//               release-ORed once the two issuing lanes' stores completed;
+//   warps 8-11  reduce (reducer units only): sum the R partial tiles in the
+//               order r = 0..R-1 from the 4-stage partial buffer (fed by the
+//               loader warp once the tile's word is (1 << R) - 1), round to
+//               bf16 and store 64-column chunks with TMA per owner piece (RS)
+//               or per view (AR) from one staging buffer.
+// Producers therefore never wait on a reduction, and the MMA never waits on
+// the partial exchange.
+// ============================================================================
+constexpr int kStages2 = 4;
+constexpr int kPStages2 = 3;
+constexpr int kAccBufs2 = 2;                         // TMEM accumulator buffers per CTA
+constexpr uint32_t kTmemCols2 = 256 * kAccBufs2;
+constexpr int kPairThreads = 384;
+constexpr uint32_t kAHalfBytes = kBM * kBK * 2;      // 16 KB: 128 rows of A
+constexpr uint32_t kBHalfBytes = (kBN / 2) * kBK * 2;  // 16 KB: 128 columns of B (two 64x64 boxes)
+constexpr uint32_t kStageTx2 = kAHalfBytes + kBHalfBytes;
+constexpr int kNumBars2 = 2 * kStages2 + 2 * kAccBufs2 + 2 * kPStages2 + 1;
+// A/B stages, partial buffer, one reduce staging buffer, two drain staging buffers
+constexpr size_t kSmemBytes2 = 1024 + (size_t)kStages2 * (kAHalfBytes + kBHalfBytes) +
+                               (size_t)kPStages2 * kSubBytes + 3 * (size_t)kSubBytes + kNumBars2 * 8 + 16;
+static_assert(kSmemBytes2 <= 232448, "shared memory budget (pair)");
+// D fp32, A/B bf16, A K-major, B MN-major, N = 256, M = 256 (pair).
+constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kBN >> 3) << 17) |
+                             ((uint32_t)(256 >> 4) << 24);
+
+struct PUnit {
+    int t;        // this CTA's 128x256 tile (row-major tile index)
+    int tm, tn, r, own;
+    bool reducer, valid;
+};
+
+__device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int u, int q) {
+    PUnit U;
+    const int tp = u / p.R;
+    const int j = u - tp * p.R;
+    const int per_group = p.group_m * p.tiles_n;
+    const int g = tp / per_group;
+    const int first = g * p.group_m;
+    const int gm = min(p.pairs_m - first, p.group_m);
+    const int in = tp - g * per_group;
+    const int tmp = first + in % gm;
+    U.tn = in / gm;
+    U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
+    int r = U.own + 1 + j;
+    while (r >= p.R) r -= p.R;
+    U.r = r;
+    U.reducer = (j == p.R - 1);
+    U.tm = 2 * tmp + q;
+    U.valid = U.tm < p.tiles_m;
+    U.t = U.tm * p.tiles_n + U.tn;
+    return U;
+}
+
+template <int ID>
+__device__ __forceinline__ void grp_bar() {
+    __syncwarp();
+    asm volatile("bar.sync %0, 128;" ::"n"(ID) : "memory");
+}
+template <int ID>
+__device__ __forceinline__ bool grp_bar_or(bool v) {
+    __syncwarp();
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(ID)
+        : "memory");
+    return r != 0;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sA = smem;
+    uint8_t* sB = sA + kStages2 * kAHalfBytes;
+    uint8_t* sP = sB + kStages2 * kBHalfBytes;
+    uint8_t* sOut = sP + kPStages2 * kSubBytes;  // reduce staging (1 buffer)
+    uint8_t* sDrain = sOut + kSubBytes;          // drain staging (2 buffers)
+    uint64_t* full = reinterpret_cast<uint64_t*>(sDrain + 2 * kSubBytes);
+    uint64_t* empty = full + kStages2;
+    uint64_t* tfull = empty + kStages2;
+    uint64_t* tempty = tfull + kAccBufs2;
+    uint64_t* pfull = tempty + kAccBufs2;
+    uint64_t* pempty = pfull + kPStages2;
+    uint64_t* mma_done = pempty + kPStages2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t q = ptx::cluster_ctarank();  // 0 = leader
+    const int cl = blockIdx.x >> 1;
+    const int G2 = gridDim.x >> 1;
+    const int nsub = (MODE == kModeRS) ? 8 : 4;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages2; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
+        for (int s = 0; s < kAccBufs2; ++s) { ptx::mbar_init(&tfull[s], 1); ptx::mbar_init(&tempty[s], 2); }
+        for (int s = 0; s < kPStages2; ++s) { ptx::mbar_init(&pfull[s], 1); ptx::mbar_init(&pempty[s], 128); }
+        ptx::mbar_init(mma_done, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_shared();
+    }
+    if (warp == 2) {
+        ptx::tmem_alloc_pair(tmem_slot, kTmemCols2);
+        ptx::tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        for (int r = 0; r < p.R; ++r) { ptx::prefetch_tmap(&p.tmA[r]); ptx::prefetch_tmap(&p.tmB[r]); }
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            const uint64_t pol = ptx::policy_evict_normal();
+            int stage = 0;
+            uint32_t ph = 0;
+            uint32_t issued = 0, issued_ph = 0;
+            bool aborted = false;
+            for (int i = 0;; ++i) {
+                if (i * G2 >= p.num_pair_units) break;
+                const int u = i * G2 + (cl + i) % G2;
+                if (u >= p.num_pair_units) continue;
+                const PUnit U = decode_pair(p, MODE, u, (int)q);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(&empty[stage], ph ^ 1u, abort_flag, p, 10, u)) { aborted = true; break; }
+                    // both CTAs' copies complete on the leader's full barrier
+                    const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
+                    if (q == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageTx2);
+                    ptx::tma_load_2d_pair(sA + stage * kAHalfBytes, &p.tmA[U.r], fb, kb * kBK, U.tm * kBM, pol);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        ptx::tma_load_2d_pair(sB + stage * kBHalfBytes + h * 8192, &p.tmB[U.r], fb,
+                                              U.tn * kBN + (int)q * 128 + h * 64, kb * kBK, pol);
+                    issued |= 1u << stage;
+                    issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
+                    if (++stage == kStages2) { stage = 0; ph ^= 1u; }
+                }
+                if (aborted) break;
+            }
+            if (q == 0) {
+                for (int s = 0; s < kStages2; ++s)
+                    if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
+            } else if (aborted) {
+                // this CTA's copies land on the leader's barriers: give them time to land
+                const uint64_t t0 = ptx::globaltimer();
+                while (ptx::globaltimer() - t0 < 50000) {}
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader only)
+        if (lane == 0 && q == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int i = 0;; ++i) {
+                if (i * G2 >= p.num_pair_units) break;
+                const int u = i * G2 + (cl + i) % G2;
+                if (u >= p.num_pair_units) continue;
+                const int buf = it % kAccBufs2;
+                const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
+                if (!wait_bar(&tempty[buf], tph ^ 1u, abort_flag, p, 11, u)) break;
+                ptx::tc_fence_after();
+                const uint32_t d = tmem_base + buf * kBN;
+                bool ok = true;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!wait_bar(&full[stage], ph, abort_flag, p, 12, u)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = ptx::smem_u32(sA + stage * kAHalfBytes);
+                    const uint32_t b0 = ptx::smem_u32(sB + stage * kBHalfBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        ptx::umma_bf16_pair(d, sdesc(a0 + kk * 32, 16, 1024), sdesc(b0 + kk * 2048, 8192, 1024),
+                                            kIdesc2, (kb | kk) != 0);
+                    ptx::umma_commit_pair_multicast(&empty[stage], 0x3);
+                    if (++stage == kStages2) { stage = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                ptx::umma_commit_pair_multicast(&tfull[buf], 0x3);
+                ++it;
+            }
+            ptx::umma_commit_pair(mma_done);
+            drain_bar(mma_done, 0, p);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ partial loader (own tile)
+        if (lane == 0) {
+            int ps = 0;
+            uint32_t pph = 0;
+            uint32_t issued = 0, issued_ph = 0;
+            const uint32_t full_mask = (p.R >= 32) ? 0xFFFFFFFFu : ((1u << p.R) - 1u);
+            for (int i = 0;; ++i) {
+                if (i * G2 >= p.num_pair_units) break;
+                const int u = i * G2 + (cl + i) % G2;
+                if (u >= p.num_pair_units) continue;
+                const PUnit U = decode_pair(p, MODE, u, (int)q);
+                if (!U.reducer || !U.valid) continue;
+                bool ok = true;
+                uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
+                if (seen != full_mask) {
+                    const uint64_t t0 = ptx::globaltimer();
+                    while (true) {
+                        ptx::nanosleep(100);
+                        seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
+                        if (seen == full_mask) break;
+                        if (*abort_flag || ptx::ld_relaxed_gpu(&p.status->code) != 0u) {
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
+                        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                            record_error(p.status, ARE_DEV_MASK_TIMEOUT, blockIdx.x, U.t, (int32_t)seen);
+                            *abort_flag = 1u;
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (!ok) break;
+                // generic-proxy acquire above, async-proxy (bulk copy) reads below
+                ptx::fence_proxy_async_global();
+                for (int j = 0; j < nsub && ok; ++j) {
+                    for (int r = 0; r < p.R; ++r) {
+                        if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&pfull[ps], kSubBytes);
+                        const uint8_t* src =
+                            p.part + ((size_t)r * p.num_tiles + U.t) * kTilePartBytes + (size_t)j * kSubBytes;
+                        ptx::bulk_load(sP + ps * kSubBytes, src, kSubBytes, &pfull[ps]);
+                        issued |= 1u << ps;
+                        issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                    }
+                }
+                if (!ok) break;
+            }
+            for (int s = 0; s < kPStages2; ++s)
+                if (issued & (1u << s)) drain_bar(&pfull[s], (issued_ph >> s) & 1u, p);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------------------------------------ drain: TMEM -> partial slot -> publish
+        const int row = threadIdx.x - 128;
+        const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
+        const bool lead = (warp == 4) && (lane == 0);
+        const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_u32(&tempty[0]), 0);
+        int it = 0;
+        bool bad = false;
+        for (int i = 0;; ++i) {
+            if (i * G2 >= p.num_pair_units) break;
+            const int u = i * G2 + (cl + i) % G2;
+            if (u >= p.num_pair_units) continue;
+            const PUnit U = decode_pair(p, MODE, u, (int)q);
+            const int buf = it % kAccBufs2;
+            const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
+            if (!wait_bar(&tfull[buf], tph, abort_flag, p, 14, u)) bad = true;
+            if (grp_bar_or<1>(bad)) { bad = true; break; }
+            ptx::tc_fence_after();
+            const uint32_t tacc = tmem_base + lane_base + buf * kBN;
+            uint8_t* gdst = p.part + ((size_t)U.r * p.num_tiles + U.t) * kTilePartBytes;
+            if (U.valid) {
+                for (int j = 0; j < nsub; ++j) {
+                    uint32_t w[32];
+                    __syncwarp();
+                    if (MODE == kModeRS) {
+                        ptx::tmem_ld32(tacc + j * 32, w);
+                    } else {
+                        uint32_t v0[32], v1[32];
+                        ptx::tmem_ld32(tacc + j * 64, v0);
+                        ptx::tmem_ld32(tacc + j * 64 + 32, v1);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            w[c] = pack_bf16x2(__uint_as_float(v0[2 * c]), __uint_as_float(v0[2 * c + 1]));
+                            w[16 + c] = pack_bf16x2(__uint_as_float(v1[2 * c]), __uint_as_float(v1[2 * c + 1]));
+                        }
+                    }
+                    if (j == nsub - 1) {
+                        // the accumulator is read: hand it back (one arrival per CTA on the leader's barrier)
+                        ptx::tc_fence_before();
+                        grp_bar<1>();
+                        if (lead) ptx::mbar_arrive_cluster(tempty_leader + (uint32_t)(buf * 8));
+                    }
+                    // swizzled smem staging -> one 16 KB bulk store per sub-tile; each staging
+                    // buffer belongs to one lane, which waits only for its own bulk group
+                    const int sb = j & 1;
+                    if (warp == 4 && lane == sb) ptx::bulk_wait_read0();
+                    grp_bar<1>();
+                    write_row_sw128(sDrain + sb * kSubBytes, row, w);
+                    ptx::fence_proxy_async_shared();
+                    grp_bar<1>();
+                    if (warp == 4 && lane == sb) {
+                        ptx::bulk_store(gdst + (size_t)j * kSubBytes, sDrain + sb * kSubBytes, kSubBytes);
+                        ptx::bulk_commit();
+                    }
+                }
+                // publish once this tile's partial is in memory: only the two issuing lanes wait
+                if (warp == 4) {
+                    if (lane < 2) {
+                        ptx::bulk_wait0();
+                        ptx::fence_proxy_async_global();
+                        __threadfence();
+                    }
+                    __syncwarp();
+                    if (lane == 0 && !((p.flags & ARE_DEBUG_SKIP_PUBLISH) && (int64_t)u == p.debug_arg))
+                        ptx::red_release_or(&p.mask[U.t], 1u << U.r);
+                }
+            } else {
+                // no such tile (odd number of tile rows): hand the accumulator back
+                ptx::tc_fence_before();
+                grp_bar<1>();
+                if (lead) ptx::mbar_arrive_cluster(tempty_leader + (uint32_t)(buf * 8));
+            }
+            ++it;
+        }
+        if (bad) *abort_flag = 1u;
+        if (warp == 4 && lane < 2) ptx::bulk_wait0();
+    } else if (warp >= 8) {
+        // ------------------------------------------------------------ reduce (reducer units of this CTA)
+        const int row = threadIdx.x - 256;
+        const bool lead = (warp == 8);
+        int ps = 0;
+        uint32_t pph = 0;
+        bool bad = false;
+        for (int i = 0;; ++i) {
+            if (i * G2 >= p.num_pair_units) break;
+            const int u = i * G2 + (cl + i) % G2;
+            if (u >= p.num_pair_units) continue;
+            const PUnit U = decode_pair(p, MODE, u, (int)q);
+            if (!U.reducer || !U.valid) continue;
+            const int row0 = U.tm * kBM;
+            for (int c = 0; c < kBN / 64; ++c) {  // 64-column output chunks
+                uint32_t outw[32];
+                if (MODE == kModeRS) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float acc[32];
+                        for (int qq = 0; qq < p.R; ++qq) {
+                            uint32_t v[32];
+                            if (!wait_bar(&pfull[ps], pph, abort_flag, p, 15, u)) bad = true;
+                            read_row_sw128(sP + ps * kSubBytes, row, v);
+                            ptx::mbar_arrive(&pempty[ps]);
+                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                            if (qq == 0) {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(v[e]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) acc[e] = acc[e] + __uint_as_float(v[e]);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) outw[16 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+                    }
+                } else {
+                    float acc[64];
+                    for (int qq = 0; qq < p.R; ++qq) {
+                        uint32_t v[32];  // 64 bf16
+                        if (!wait_bar(&pfull[ps], pph, abort_flag, p, 15, u)) bad = true;
+                        read_row_sw128(sP + ps * kSubBytes, row, v);
+                        ptx::mbar_arrive(&pempty[ps]);
+                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        if (qq == 0) {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                acc[2 * e] = __uint_as_float(v[e] << 16);
+                                acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) {
+                                acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
+                                acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) outw[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+                }
+                const int sb = 0;  // one staging buffer: lane 0 issues and waits for its stores
+                if (lead && lane == 0) ptx::bulk_wait_read0();
+                if (grp_bar_or<2>(bad)) { bad = true; break; }
+                write_row_sw128(sOut, row, outw);
+                ptx::fence_proxy_async_shared();
+                grp_bar<2>();
+                if (lead && lane == 0) {
+                    const int x = U.tn * kBN + c * 64;
+                    if (x < p.N) {
+                        if (MODE == kModeRS) {
+                            // owner-boundary flush: one store per (segment piece, H-row box)
+                            const int row_end = min(row0 + kBM, p.M);
+                            for (int r0 = row0; r0 < row_end;) {
+                                const int s = r0 / p.S;
+                                const int e = min((s + 1) * p.S, row_end);
+                                for (int rb = r0; rb < e; rb += p.H)
+                                    ptx::tma_store_2d(&p.tmOut[s], sOut + sb * kSubBytes + (rb - row0) * 128, x,
+                                                      rb - s * p.S);
+                                r0 = e;
+                            }
+                        } else {
+                            for (int v = 0; v < p.nviews; ++v)
+                                ptx::tma_store_2d(&p.tmOut[v], sOut + sb * kSubBytes, x, row0);
+                        }
+                        ptx::bulk_commit();
+                    }
+                }
+            }
+            if (bad) break;
+            if (lead && lane == 0) {
+                if (MODE == kModeRS && (p.flags & ARE_DEBUG_LOG_PIECES)) {
+                    int32_t* log = p.pieces + (size_t)U.t * kPieceWords;
+                    const int row_end = min(row0 + kBM, p.M);
+                    int n = 0;
+                    for (int r0 = row0; r0 < row_end && n < (kPieceWords - 3) / 3;) {
+                        const int s = r0 / p.S;
+                        const int e = min((s + 1) * p.S, row_end);
+                        log[3 + 3 * n] = s; log[4 + 3 * n] = r0; log[5 + 3 * n] = e;
+                        ++n;
+                        r0 = e;
+                    }
+                    log[0] = U.tm; log[1] = U.tn; log[2] = n;
+                }
+                // re-arm the tile's mask word for the next call
+                if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
+            }
+        }
+        if (bad) *abort_flag = 1u;
+        if (lead && lane == 0) ptx::bulk_wait0();
+    }
+
+    __syncwarp();
+    ptx::tc_fence_before();
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    if (warp == 2) {
+        __syncwarp();
+        ptx::tmem_dealloc_pair(tmem_base, kTmemCols2);
     }
 }
 
@@ -538,6 +1008,23 @@ cudaError_t get_encode() {
 
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
+int g_pair_clusters = -1;
+
+cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes2;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
 cudaError_t gemm_prepare_kernels() {
     cudaError_t e = cudaFuncSetAttribute(gemm_reduce_kernel<kModeRS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
@@ -545,8 +1032,26 @@ cudaError_t gemm_prepare_kernels() {
     e = cudaFuncSetAttribute(gemm_reduce_kernel<kModeAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_pair_kernel<kModeRS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes2);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_pair_kernel<kModeAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes2);
+    if (e != cudaSuccess) return e;
+    if (g_pair_clusters < 0) {
+        // co-resident clusters bound the persistent grid (every cluster must be running)
+        int n_rs = 0, n_ar = 0;
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg = pair_config(2 * 1024, nullptr, attr);
+        if (cudaOccupancyMaxActiveClusters(&n_rs, (void*)gemm_pair_kernel<kModeRS>, &cfg) != cudaSuccess) n_rs = 0;
+        if (cudaOccupancyMaxActiveClusters(&n_ar, (void*)gemm_pair_kernel<kModeAR>, &cfg) != cudaSuccess) n_ar = 0;
+        cudaGetLastError();
+        g_pair_clusters = n_rs < n_ar ? n_rs : n_ar;
+    }
     return get_encode();
 }
+
+int gemm_pair_max_clusters() { return g_pair_clusters < 0 ? 0 : g_pair_clusters; }
 
 // bf16 [outer, inner] row-major, 128B-swizzled boxes of box_inner x box_outer.
 cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
@@ -561,6 +1066,15 @@ cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uin
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t launch_gemm_pair(const GemmParams& p, int mode, int grid, cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pair_config(grid, stream, attr);
+    cudaError_t e = (mode == kModeRS) ? cudaLaunchKernelEx(&cfg, gemm_pair_kernel<kModeRS>, p)
+                                      : cudaLaunchKernelEx(&cfg, gemm_pair_kernel<kModeAR>, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_reduce(const GemmParams& p, int mode, int grid, cudaStream_t stream) {

@@ -103,7 +103,8 @@ enum {
     ARE_DEBUG_LOG_PIECES = 2u,    /* record the owner pieces each GEMM+RS reducer stored */
     ARE_DEBUG_COUNT_CANON = 4u,   /* count staged words canonicalised from -0.0 to +0.0 */
     ARE_DEBUG_SKIP_PUBLISH = 8u,  /* GEMM: work unit `debug_arg` never sets its ready bit */
-    ARE_DEBUG_SKIP_STAGE = 16u    /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
+    ARE_DEBUG_SKIP_STAGE = 16u,   /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
+    ARE_DEBUG_SINGLE_CTA = 32u    /* GEMM: use the one-CTA kernel even where the CTA-pair kernel applies */
 };
 
 /* Device status word, see are_get_device_status(). */
