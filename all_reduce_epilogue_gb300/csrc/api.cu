@@ -192,6 +192,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     p->num_units = (int)(T * R);
     p->num_kb = (int)ceil_div(K, kBK);
     p->pairs_m = (int)((tiles_m + 1) / 2);
+    p->block_tiles = 0;
     p->num_pair_units = (int)(p->pairs_m * tiles_n * R);
     p->flags = ws->debug_flags;
     p->debug_arg = ws->debug_arg;
@@ -201,6 +202,15 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     const int clusters = gemm_pair_max_clusters();
     if (tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA)) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
+        // GEMM+RS: run the ranks block by block (two waves of tile pairs per block) so a
+        // wave streams one or two ranks' operands; GEMM+AR keeps the ranks innermost (its
+        // reductions write R views and are better spread over the waves)
+        if (mode == kModeRS) p->block_tiles = 2 * clusters;
+        if (p->block_tiles > 0) {
+            const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
+            const int64_t blocks = (num_pairs + p->block_tiles - 1) / p->block_tiles;
+            p->num_pair_units = (int)(blocks * p->block_tiles * R);
+        }
         const int grid = 2 * (int)std::min<int64_t>(p->num_pair_units, clusters);
         e = launch_gemm_pair(*p, mode, grid, s);
     } else {

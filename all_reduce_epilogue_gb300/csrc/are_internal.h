@@ -97,6 +97,7 @@ struct GemmParams {
     int nviews;          // distinct output views (AR)
     int tiles_m, tiles_n, num_tiles, num_units, num_kb;
     int pairs_m, num_pair_units;  // CTA-pair kernel: 256-row tile pairs, R units per pair
+    int block_tiles;     // CTA-pair kernel: tile pairs per rank block (0 = ranks innermost)
     int group_m;         // tile raster: rows of tiles (pairs) per group
     uint32_t flags;
     int64_t debug_arg;

@@ -575,12 +575,36 @@ struct PUnit {
     int t;        // this CTA's 128x256 tile (row-major tile index)
     int tm, tn, r, own;
     bool reducer, valid;
+    bool pad;     // padding unit of the last rank block: skipped by every role
 };
 
+// Pair-unit order.  block_tiles == 0: the R units of a tile pair are
+// consecutive (ranks innermost).  block_tiles == B: tile pairs are taken in
+// blocks of B (in raster order) and a block's units run rank by rank: the j-th
+// unit of every pair in the block, then the (j+1)-th, so a wave streams the
+// operands of one or two ranks; the reducer (j = R-1) stays last per pair.
+// Units past the last pair (padding of the last block) are not valid.
 __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int u, int q) {
     PUnit U;
-    const int tp = u / p.R;
-    const int j = u - tp * p.R;
+    int tp, j;
+    if (p.block_tiles > 0) {
+        const int per_block = p.block_tiles * p.R;
+        const int blk = u / per_block;
+        const int rem = u - blk * per_block;
+        j = rem / p.block_tiles;
+        tp = blk * p.block_tiles + (rem - j * p.block_tiles);
+    } else {
+        tp = u / p.R;
+        j = u - tp * p.R;
+    }
+    const int num_pairs = p.pairs_m * p.tiles_n;
+    U.pad = tp >= num_pairs;
+    if (U.pad) {  // padding unit: no tile
+        U.t = 0; U.tm = p.tiles_m; U.tn = 0; U.r = 0; U.own = 0;
+        U.reducer = false;
+        U.valid = false;
+        return U;
+    }
     const int per_group = p.group_m * p.tiles_n;
     const int g = tp / per_group;
     const int first = g * p.group_m;
@@ -677,6 +701,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 const int u = i * G2 + (cl + i) % G2;
                 if (u >= p.num_pair_units) continue;
                 const PUnit U = decode_pair(p, MODE, u, (int)q);
+                if (U.pad) continue;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!wait_bar(&empty[stage], ph ^ 1u, abort_flag, p, 10, u)) { aborted = true; break; }
                     // both CTAs' copies complete on the leader's full barrier
@@ -712,6 +737,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (i * G2 >= p.num_pair_units) break;
                 const int u = i * G2 + (cl + i) % G2;
                 if (u >= p.num_pair_units) continue;
+                if (decode_pair(p, MODE, u, 0).pad) continue;
                 const int buf = it % kAccBufs2;
                 const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
                 if (!wait_bar(&tempty[buf], tph ^ 1u, abort_flag, p, 11, u)) break;
@@ -804,6 +830,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             const int u = i * G2 + (cl + i) % G2;
             if (u >= p.num_pair_units) continue;
             const PUnit U = decode_pair(p, MODE, u, (int)q);
+            if (U.pad) continue;
             const int buf = it % kAccBufs2;
             const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
             if (!wait_bar(&tfull[buf], tph, abort_flag, p, 14, u)) bad = true;

@@ -154,22 +154,26 @@ def test_masks_and_owner_pieces_bit_exact(oracle):
             assert np.all(ws.snapshot(are.SNAP_MASKS, T * 4).view(np.uint32) == 0)
 
 
-def test_unpublished_tile_times_out_and_reset_recovers(oracle):
+@pytest.mark.parametrize("single_cta", [True, False])
+def test_unpublished_tile_times_out_and_reset_recovers(oracle, single_cta):
     """A producer that never sets its ready bit makes the tile's reducer time
-    out: the status names the tile, every CTA returns, and a reset recovers."""
+    out: the status names the tile, every CTA returns, and a reset recovers.
+    Unit 0 is the first producer of tile 0 for the one-CTA kernel, and of the
+    first tile pair (tiles 0 and N/256) for the CTA-pair kernel."""
     need_gpu()
     import all_reduce_epilogue_gb300 as are
     R, M, N, K = 4, 256, 512, 128
     A, B = synth.gemm_inputs(R, M, N, K, 8)
+    base = are.DEBUG_SINGLE_CTA if single_cta else 0
     with make_ws(timeout_ns=20_000_000) as ws:
-        ws.set_debug(are.DEBUG_SKIP_PUBLISH, 0)  # unit 0 = first producer of tile 0
+        ws.set_debug(base | are.DEBUG_SKIP_PUBLISH, 0)
         import torch
         out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         are.gemm_rs([dev_bf16(a) for a in A], [dev_bf16(b) for b in B], out, ws)
         st = ws.device_status()
         assert st["status"] == are.ETIMEOUT and st["code"] == are.DEV_MASK_TIMEOUT, st
-        assert st["a"] == 0
-        ws.set_debug(0)
+        assert st["a"] in ((0,) if single_cta else (0, N // 256)), st
+        ws.set_debug(base)
         ws.reset()
         got = host_f32(run_rs(ws, A, B))
     check_close(got, oracle.gemm_rs(A, B), "after reset")
@@ -248,3 +252,30 @@ def test_large_gemm_rs_sampled_and_deterministic(oracle):
         assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)), "not deterministic"
         got = host_f32(o1)[rows]
     check_close(got, oracle.gemm_rs(A, B, rows), "large gemm_rs sampled")
+
+
+@pytest.mark.parametrize("mode,R,M,N,K", [("rs", 8, 1024, 1024, 512), ("rs", 3, 384, 520, 136), ("ar", 8, 640, 7168, 256),
+                                          ("ar", 2, 512, 1024, 1024)])
+def test_pair_kernel_matches_single_cta_kernel(mode, R, M, N, K):
+    """The CTA-pair kernel (256-row tiles, cta_group::2) and the one-CTA kernel
+    compute each output element with the same operations in the same order,
+    so their outputs are bitwise identical (several waves, an odd number of
+    tile rows where one CTA of the last pair has no tile)."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    A, B = synth.gemm_inputs(R, M, N, K, 321 + M + R)
+    dA = [dev_bf16(a) for a in A]
+    dB = [dev_bf16(b) for b in B]
+    outs = []
+    for flags in (0, are.DEBUG_SINGLE_CTA):
+        with make_ws(M_max=M, N_max=N, K_max=K, debug_flags=flags) as ws:
+            out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            if mode == "rs":
+                are.gemm_rs(dA, dB, out, ws)
+            else:
+                are.gemm_ar(dA, dB, [out] * R, ws)
+            assert ws.device_status()["code"] == 0
+            outs.append(host_bits(out))
+    assert np.array_equal(outs[0], outs[1])
