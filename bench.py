@@ -46,9 +46,11 @@ EPS = 1e-6
 # Fallback denominators (one earlier GB300 measurement), used only when the
 # measured peaks file is absent.
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM traffic per launch (read + write bytes) from one ncu capture of each
-# kernel (see profiles/); None until captured for the current kernel source.
-NCU_TRAFFIC = {"gemm_rs": None, "gemm_ar": None, "allreduce_rmsnorm": None}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# each part's kernel at this workload, from one ncu capture of a bench step
+# (profiles/launch_list_bench_step.md).  Set back to None whenever that kernel's
+# source changes, until it is captured again.
+NCU_TRAFFIC = {"gemm_rs": 9813.7e6, "gemm_ar": 3530.8e6, "allreduce_rmsnorm": 640.0e6}
 
 
 # --------------------------------------------------------------------------- work model
@@ -367,12 +369,12 @@ def run_gpu(args):
     peak_t = peaks["bf16_tflops_sustained"]
     flops_rs, _ = work("gemm_rs")
     ach_rs = flops_rs / (per_ms["gemm_rs"] * 1e-3) / 1e12
-    roofline = {"kernel": "gemm_reduce_kernel<RS> (gemm_rs)", "bound": "tensor", "achieved": ach_rs,
+    roofline = {"kernel": "gemm_pair_kernel<RS> (gemm_rs)", "bound": "tensor", "achieved": ach_rs,
                 "peak": peak_t, "unit": "TFLOP/s", "frac": ach_rs / peak_t, "traffic": NCU_TRAFFIC["gemm_rs"],
                 "peak_source": f"{source} bf16 sustained", "note": f"of {source}"}
     _, bytes_n = work("allreduce_rmsnorm")
     ach_n = bytes_n / (per_ms["allreduce_rmsnorm"] * 1e-3) / 1e9
-    roofline_ar = {"kernel": "ar_rmsnorm_kernel (allreduce_rmsnorm)", "bound": "hbm", "achieved": ach_n,
+    roofline_ar = {"kernel": "ar_rmsnorm_kernel<4> (allreduce_rmsnorm)", "bound": "hbm", "achieved": ach_n,
                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach_n / peaks["hbm_gbs"],
                    "traffic": NCU_TRAFFIC["allreduce_rmsnorm"], "peak_source": f"{source} HBM copy",
                    "note": f"of {source}"}
