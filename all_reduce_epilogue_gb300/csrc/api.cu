@@ -46,7 +46,7 @@ struct are_ws {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 200ull * 1000 * 1000;
-constexpr size_t kCounterWords = 4;
+constexpr size_t kCounterWords = 16;
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -179,6 +179,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     p->mask = ws->d_mask;
     p->status = ws->d_status;
     p->pieces = ws->d_pieces;
+    p->counters = ws->d_counters;
     p->R = R;
     p->M = (int)M;
     p->N = (int)N;

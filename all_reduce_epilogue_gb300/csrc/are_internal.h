@@ -90,6 +90,7 @@ struct GemmParams {
     uint32_t* mask;      // [T]
     DevStatus* status;
     int32_t* pieces;     // debug piece log [T][kPieceWords]
+    unsigned long long* counters;  // debug counters (wait profile)
     int R;
     int M, N, K;
     int S;               // owner segment rows (RS)

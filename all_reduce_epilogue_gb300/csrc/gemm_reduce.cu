@@ -116,6 +116,20 @@ __device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, const Gem
     }
 }
 
+// wait_bar that, under ARE_DEBUG_WAIT_PROFILE, adds the SM cycles spent
+// waiting to `acc`.
+__device__ __forceinline__ bool wait_bar_prof(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                              const GemmParams& p, int id, int unit, uint64_t& acc) {
+    if (!(p.flags & ARE_DEBUG_WAIT_PROFILE)) return wait_bar(bar, parity, abort_flag, p, id, unit);
+    const uint64_t t0 = clock64();
+    const bool ok = wait_bar(bar, parity, abort_flag, p, id, unit);
+    acc += (uint64_t)(clock64() - t0);
+    return ok;
+}
+__device__ __forceinline__ void prof_add(const GemmParams& p, int slot, uint64_t v) {
+    if ((p.flags & ARE_DEBUG_WAIT_PROFILE) && v) atomicAdd(&p.counters[slot], (unsigned long long)v);
+}
+
 // Named barriers are .aligned: every lane of a warp must arrive together, so
 // each helper first reconverges the warp (lanes that ran a single-lane branch,
 // such as issuing a store or an arrive, would otherwise arrive late and be
@@ -696,6 +710,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             uint32_t ph = 0;
             uint32_t issued = 0, issued_ph = 0;
             bool aborted = false;
+            uint64_t w_empty = 0;
             for (int i = 0;; ++i) {
                 if (i * G2 >= p.num_pair_units) break;
                 const int u = i * G2 + (cl + i) % G2;
@@ -703,7 +718,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 const PUnit U = decode_pair(p, MODE, u, (int)q);
                 if (U.pad) continue;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(&empty[stage], ph ^ 1u, abort_flag, p, 10, u)) { aborted = true; break; }
+                    if (!wait_bar_prof(&empty[stage], ph ^ 1u, abort_flag, p, 10, u, w_empty)) {
+                        aborted = true;
+                        break;
+                    }
                     // both CTAs' copies complete on the leader's full barrier
                     const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
                     if (q == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageTx2);
@@ -718,6 +736,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 }
                 if (aborted) break;
             }
+            prof_add(p, 1, w_empty);
+            prof_add(p, 8, 1);
             if (q == 0) {
                 for (int s = 0; s < kStages2; ++s)
                     if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
@@ -733,6 +753,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             int stage = 0;
             uint32_t ph = 0;
             int it = 0;
+            uint64_t w_full = 0, w_tempty = 0;
+            const uint64_t c_start = clock64();
             for (int i = 0;; ++i) {
                 if (i * G2 >= p.num_pair_units) break;
                 const int u = i * G2 + (cl + i) % G2;
@@ -740,12 +762,12 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (decode_pair(p, MODE, u, 0).pad) continue;
                 const int buf = it % kAccBufs2;
                 const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
-                if (!wait_bar(&tempty[buf], tph ^ 1u, abort_flag, p, 11, u)) break;
+                if (!wait_bar_prof(&tempty[buf], tph ^ 1u, abort_flag, p, 11, u, w_tempty)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + buf * kBN;
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(&full[stage], ph, abort_flag, p, 12, u)) { ok = false; break; }
+                    if (!wait_bar_prof(&full[stage], ph, abort_flag, p, 12, u, w_full)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t a0 = ptx::smem_u32(sA + stage * kAHalfBytes);
                     const uint32_t b0 = ptx::smem_u32(sB + stage * kBHalfBytes);
@@ -762,6 +784,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             }
             ptx::umma_commit_pair(mma_done);
             drain_bar(mma_done, 0, p);
+            prof_add(p, 2, w_full);
+            prof_add(p, 3, w_tempty);
+            prof_add(p, 4, (uint64_t)(clock64() - c_start));
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ partial loader (own tile)
@@ -770,6 +795,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             uint32_t pph = 0;
             uint32_t issued = 0, issued_ph = 0;
             const uint32_t full_mask = (p.R >= 32) ? 0xFFFFFFFFu : ((1u << p.R) - 1u);
+            uint64_t w_mask = 0;
             for (int i = 0;; ++i) {
                 if (i * G2 >= p.num_pair_units) break;
                 const int u = i * G2 + (cl + i) % G2;
@@ -779,6 +805,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 bool ok = true;
                 uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
                 if (seen != full_mask) {
+                    const uint64_t c0 = clock64();
                     const uint64_t t0 = ptx::globaltimer();
                     while (true) {
                         ptx::nanosleep(100);
@@ -796,6 +823,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                             break;
                         }
                     }
+                    w_mask += (uint64_t)(clock64() - c0);
                 }
                 if (!ok) break;
                 // generic-proxy acquire above, async-proxy (bulk copy) reads below
@@ -814,6 +842,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 }
                 if (!ok) break;
             }
+            prof_add(p, 6, w_mask);
             for (int s = 0; s < kPStages2; ++s)
                 if (issued & (1u << s)) drain_bar(&pfull[s], (issued_ph >> s) & 1u, p);
         }
@@ -825,6 +854,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_u32(&tempty[0]), 0);
         int it = 0;
         bool bad = false;
+        uint64_t w_tfull = 0;
         for (int i = 0;; ++i) {
             if (i * G2 >= p.num_pair_units) break;
             const int u = i * G2 + (cl + i) % G2;
@@ -833,7 +863,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             if (U.pad) continue;
             const int buf = it % kAccBufs2;
             const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
-            if (!wait_bar(&tfull[buf], tph, abort_flag, p, 14, u)) bad = true;
+            if (!wait_bar_prof(&tfull[buf], tph, abort_flag, p, 14, u, w_tfull)) bad = true;
             if (grp_bar_or<1>(bad)) { bad = true; break; }
             ptx::tc_fence_after();
             const uint32_t tacc = tmem_base + lane_base + buf * kBN;
@@ -893,6 +923,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             ++it;
         }
         if (bad) *abort_flag = 1u;
+        if (lead) prof_add(p, 5, w_tfull);
         if (warp == 4 && lane < 2) ptx::bulk_wait0();
     } else if (warp >= 8) {
         // ------------------------------------------------------------ reduce (reducer units of this CTA)
@@ -901,6 +932,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         int ps = 0;
         uint32_t pph = 0;
         bool bad = false;
+        uint64_t w_pfull = 0;
         for (int i = 0;; ++i) {
             if (i * G2 >= p.num_pair_units) break;
             const int u = i * G2 + (cl + i) % G2;
@@ -916,7 +948,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         float acc[32];
                         for (int qq = 0; qq < p.R; ++qq) {
                             uint32_t v[32];
-                            if (!wait_bar(&pfull[ps], pph, abort_flag, p, 15, u)) bad = true;
+                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
                             read_row_sw128(sP + ps * kSubBytes, row, v);
                             ptx::mbar_arrive(&pempty[ps]);
                             if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
@@ -935,7 +967,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     float acc[64];
                     for (int qq = 0; qq < p.R; ++qq) {
                         uint32_t v[32];  // 64 bf16
-                        if (!wait_bar(&pfull[ps], pph, abort_flag, p, 15, u)) bad = true;
+                        if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
                         read_row_sw128(sP + ps * kSubBytes, row, v);
                         ptx::mbar_arrive(&pempty[ps]);
                         if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
@@ -1004,6 +1036,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             }
         }
         if (bad) *abort_flag = 1u;
+        if (lead && lane == 0) prof_add(p, 7, w_pfull);
         if (lead && lane == 0) ptx::bulk_wait0();
     }
 

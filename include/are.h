@@ -104,7 +104,8 @@ enum {
     ARE_DEBUG_COUNT_CANON = 4u,   /* count staged words canonicalised from -0.0 to +0.0 */
     ARE_DEBUG_SKIP_PUBLISH = 8u,  /* GEMM: work unit `debug_arg` never sets its ready bit */
     ARE_DEBUG_SKIP_STAGE = 16u,   /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
-    ARE_DEBUG_SINGLE_CTA = 32u    /* GEMM: use the one-CTA kernel even where the CTA-pair kernel applies */
+    ARE_DEBUG_SINGLE_CTA = 32u,   /* GEMM: use the one-CTA kernel even where the CTA-pair kernel applies */
+    ARE_DEBUG_WAIT_PROFILE = 64u  /* GEMM (CTA-pair kernel): add each role's waiting SM cycles to the counters */
 };
 
 /* Device status word, see are_get_device_status(). */
@@ -127,7 +128,12 @@ enum {
     ARE_SNAP_MASKS = 1,    /* uint32 per tile (tile index in the kernel's work order) */
     ARE_SNAP_STAGING = 2,  /* fp32 staging words, row-major [M, N] of the last AR+RMSNorm call */
     ARE_SNAP_PIECES = 3,   /* int32 x 64 per tile: tile_m, tile_n, count, then (segment, begin, end) x count */
-    ARE_SNAP_COUNTERS = 4  /* uint64 x 4: [0] canonicalised words */
+    ARE_SNAP_COUNTERS = 4  /* uint64 x 16: [0] canonicalised words; with ARE_DEBUG_WAIT_PROFILE, summed over
+                              the CTAs, in SM cycles: [1] TMA producer waiting for a free stage, [2] MMA
+                              waiting for operands, [3] MMA waiting for a free accumulator, [4] MMA thread
+                              from its first wait to its last commit, [5] drain waiting for an accumulator,
+                              [6] loader waiting for tile masks, [7] reduce waiting for partial sub-tiles,
+                              [8] CTAs counted */
 };
 
 typedef struct are_ws are_ws;

@@ -279,3 +279,31 @@ def test_pair_kernel_matches_single_cta_kernel(mode, R, M, N, K):
             assert ws.device_status()["code"] == 0
             outs.append(host_bits(out))
     assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.gpu
+def test_wait_profile_counts_and_leaves_results_unchanged():
+    """With the wait profile on, the pair kernel's output is bitwise the same
+    and every role has reported: one producer per CTA, the MMA span covers the
+    MMA waits, and no wait fraction exceeds its span."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    R, M, N, K = 4, 1024, 1024, 512
+    A, B = synth.gemm_inputs(R, M, N, K, 777)
+    dA = [dev_bf16(a) for a in A]
+    dB = [dev_bf16(b) for b in B]
+    with make_ws(M_max=M, N_max=N, K_max=K) as ws:
+        out0 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        are.gemm_rs(dA, dB, out0, ws)
+        ws.reset()
+        ws.set_debug(are.DEBUG_WAIT_PROFILE)
+        out1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        are.gemm_rs(dA, dB, out1, ws)
+        assert ws.device_status()["code"] == 0
+        c = ws.snapshot(are.SNAP_COUNTERS, 128).view(np.uint64)
+    assert np.array_equal(host_bits(out0), host_bits(out1))
+    ctas = int(c[8])
+    assert ctas >= 2 and ctas % 2 == 0
+    assert c[4] > 0 and c[2] + c[3] <= c[4]
