@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 // ============================================================================
 // CTA-pair variant: tcgen05.mma.cta_group::2 computes a 256x256 tile per CTA
 // pair (cluster of 2).  Each CTA stages its own 128 rows of A and its own 128
-// columns of B (32 KB per k-block, 4 stages) and holds its 128x256 half of the
+// columns of B (32 KB per k-block, 5 stages) and holds its 128x256 half of the
 // accumulator in its own TMEM; the leader (cluster rank 0) issues the MMAs.
 // Each CTA's half is one 128x256 output tile with its own mask word and
 // partial slot; the pair computes the same rank r for both halves, and the
@@ -555,21 +555,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 // mod R for GEMM+AR) reduces both halves.
 //
 // The epilogue is split so that no reduction ever holds TMEM:
-//   warps 4-7   drain: TMEM -> registers -> swizzled staging -> 16 KB bulk
+//   warps 4-7   drain: TMEM -> registers -> swizzled staging -> 8 KB bulk
 //               stores into the unit's partial slot (fp32 for RS, bf16 for
 //               AR; the reducer's own partial too); the accumulator goes back
 //               to the MMA as soon as it is read, and the unit's bit is
 //               release-ORed once the two issuing lanes' stores completed;
 //   warps 8-11  reduce (reducer units only): sum the R partial tiles in the
-//               order r = 0..R-1 from the 4-stage partial buffer (fed by the
+//               order r = 0..R-1 from the 3-stage partial buffer (fed by the
 //               loader warp once the tile's word is (1 << R) - 1), round to
 //               bf16 and store 64-column chunks with TMA per owner piece (RS)
 //               or per view (AR) from one staging buffer.
 // Producers therefore never wait on a reduction, and the MMA never waits on
 // the partial exchange.
 // ============================================================================
-constexpr int kStages2 = 4;
+constexpr int kStages2 = 5;
 constexpr int kPStages2 = 3;
+// Partial sub-tile of the pair kernel: 128 rows x 64 bytes (16 fp32 or 32 bf16
+// columns), 64-byte swizzled.  Small sub-tiles keep the partial buffer and the
+// drain staging at 40 KB, which leaves room for five mainloop stages.
+constexpr uint32_t kPSub2 = 8192;
 constexpr int kAccBufs2 = 2;                         // TMEM accumulator buffers per CTA
 constexpr uint32_t kTmemCols2 = 256 * kAccBufs2;
 constexpr int kPairThreads = 384;
@@ -579,7 +583,8 @@ constexpr uint32_t kStageTx2 = kAHalfBytes + kBHalfBytes;
 constexpr int kNumBars2 = 2 * kStages2 + 2 * kAccBufs2 + 2 * kPStages2 + 1;
 // A/B stages, partial buffer, one reduce staging buffer, two drain staging buffers
 constexpr size_t kSmemBytes2 = 1024 + (size_t)kStages2 * (kAHalfBytes + kBHalfBytes) +
-                               (size_t)kPStages2 * kSubBytes + 3 * (size_t)kSubBytes + kNumBars2 * 8 + 16;
+                               (size_t)kPStages2 * kPSub2 + (size_t)kSubBytes + 2 * (size_t)kPSub2 +
+                               kNumBars2 * 8 + 16;
 static_assert(kSmemBytes2 <= 232448, "shared memory budget (pair)");
 // D fp32, A/B bf16, A K-major, B MN-major, N = 256, M = 256 (pair).
 constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(kBN >> 3) << 17) |
@@ -637,6 +642,27 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
     return U;
 }
 
+// Row `row` of a 128 x 64-byte sub-tile: 16-byte chunk c lives at chunk
+// c ^ ((row >> 1) & 3), so the 32 rows of a warp touching one chunk column
+// spread evenly over the banks (four wavefronts per 512 bytes, the minimum).
+// H selects which 16 words of `w` (columns 16H..16H+15 of a 32-word row).
+template <int H>
+__device__ __forceinline__ void write_half_sw64(uint8_t* base, int row, const uint32_t (&w)[32]) {
+    uint8_t* rp = base + row * 64;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(rp + ((c ^ ((row >> 1) & 3)) << 4)) =
+            make_uint4(w[16 * H + 4 * c], w[16 * H + 4 * c + 1], w[16 * H + 4 * c + 2], w[16 * H + 4 * c + 3]);
+}
+__device__ __forceinline__ void read_row_sw64(const uint8_t* base, int row, uint32_t (&w)[16]) {
+    const uint8_t* rp = base + row * 64;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ ((row >> 1) & 3)) << 4));
+        w[4 * c] = v.x; w[4 * c + 1] = v.y; w[4 * c + 2] = v.z; w[4 * c + 3] = v.w;
+    }
+}
+
 template <int ID>
 __device__ __forceinline__ void grp_bar() {
     __syncwarp();
@@ -661,9 +687,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     uint8_t* sA = smem;
     uint8_t* sB = sA + kStages2 * kAHalfBytes;
     uint8_t* sP = sB + kStages2 * kBHalfBytes;
-    uint8_t* sOut = sP + kPStages2 * kSubBytes;  // reduce staging (1 buffer)
-    uint8_t* sDrain = sOut + kSubBytes;          // drain staging (2 buffers)
-    uint64_t* full = reinterpret_cast<uint64_t*>(sDrain + 2 * kSubBytes);
+    uint8_t* sOut = sP + kPStages2 * kPSub2;     // reduce staging (1 buffer)
+    uint8_t* sDrain = sOut + kSubBytes;          // drain staging (2 buffers of kPSub2)
+    uint64_t* full = reinterpret_cast<uint64_t*>(sDrain + 2 * kPSub2);
     uint64_t* empty = full + kStages2;
     uint64_t* tfull = empty + kStages2;
     uint64_t* tempty = tfull + kAccBufs2;
@@ -678,7 +704,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     const uint32_t q = ptx::cluster_ctarank();  // 0 = leader
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
-    const int nsub = (MODE == kModeRS) ? 8 : 4;
+    const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
@@ -828,13 +854,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (!ok) break;
                 // generic-proxy acquire above, async-proxy (bulk copy) reads below
                 ptx::fence_proxy_async_global();
-                for (int j = 0; j < nsub && ok; ++j) {
+                for (int j = 0; j < 2 * nsub && ok; ++j) {
                     for (int r = 0; r < p.R; ++r) {
                         if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(&pfull[ps], kSubBytes);
+                        ptx::mbar_arrive_expect_tx(&pfull[ps], kPSub2);
                         const uint8_t* src =
-                            p.part + ((size_t)r * p.num_tiles + U.t) * kTilePartBytes + (size_t)j * kSubBytes;
-                        ptx::bulk_load(sP + ps * kSubBytes, src, kSubBytes, &pfull[ps]);
+                            p.part + ((size_t)r * p.num_tiles + U.t) * kTilePartBytes + (size_t)j * kPSub2;
+                        ptx::bulk_load(sP + ps * kPSub2, src, kPSub2, &pfull[ps]);
                         issued |= 1u << ps;
                         issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
                         if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
@@ -890,16 +916,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         grp_bar<1>();
                         if (lead) ptx::mbar_arrive_cluster(tempty_leader + (uint32_t)(buf * 8));
                     }
-                    // swizzled smem staging -> one 16 KB bulk store per sub-tile; each staging
-                    // buffer belongs to one lane, which waits only for its own bulk group
-                    const int sb = j & 1;
-                    if (warp == 4 && lane == sb) ptx::bulk_wait_read0();
+                    // the 128-byte row chunk becomes partial sub-tiles 2j and 2j+1: swizzled smem
+                    // staging -> one 8 KB bulk store each; staging buffer b belongs to lane b,
+                    // which waits only for its own bulk group before refilling it
+                    if (warp == 4 && lane < 2) ptx::bulk_wait_read0();
                     grp_bar<1>();
-                    write_row_sw128(sDrain + sb * kSubBytes, row, w);
+                    write_half_sw64<0>(sDrain, row, w);
+                    write_half_sw64<1>(sDrain + kPSub2, row, w);
                     ptx::fence_proxy_async_shared();
                     grp_bar<1>();
-                    if (warp == 4 && lane == sb) {
-                        ptx::bulk_store(gdst + (size_t)j * kSubBytes, sDrain + sb * kSubBytes, kSubBytes);
+                    if (warp == 4 && lane < 2) {
+                        ptx::bulk_store(gdst + (size_t)(2 * j + lane) * kPSub2, sDrain + lane * kPSub2, kPSub2);
                         ptx::bulk_commit();
                     }
                 }
@@ -944,49 +971,52 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 uint32_t outw[32];
                 if (MODE == kModeRS) {
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float acc[32];
+                    for (int h = 0; h < 4; ++h) {  // partial sub-tile 4c + h: columns 16h..16h+15 of the chunk
+                        float acc[16];
                         for (int qq = 0; qq < p.R; ++qq) {
-                            uint32_t v[32];
+                            uint32_t v[16];
                             if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
-                            read_row_sw128(sP + ps * kSubBytes, row, v);
+                            read_row_sw64(sP + ps * kPSub2, row, v);
                             ptx::mbar_arrive(&pempty[ps]);
                             if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
                             if (qq == 0) {
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) acc[e] = __uint_as_float(v[e]);
+                                for (int e = 0; e < 16; ++e) acc[e] = __uint_as_float(v[e]);
                             } else {
 #pragma unroll
-                                for (int e = 0; e < 32; ++e) acc[e] = acc[e] + __uint_as_float(v[e]);
+                                for (int e = 0; e < 16; ++e) acc[e] = acc[e] + __uint_as_float(v[e]);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) outw[8 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {  // partial sub-tile 2c + h: columns 32h..32h+31 of the chunk
+                        float acc[32];
+                        for (int qq = 0; qq < p.R; ++qq) {
+                            uint32_t v[16];  // 32 bf16
+                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
+                            read_row_sw64(sP + ps * kPSub2, row, v);
+                            ptx::mbar_arrive(&pempty[ps]);
+                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                            if (qq == 0) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    acc[2 * e] = __uint_as_float(v[e] << 16);
+                                    acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
+                                    acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
+                                }
                             }
                         }
 #pragma unroll
                         for (int e = 0; e < 16; ++e) outw[16 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
                     }
-                } else {
-                    float acc[64];
-                    for (int qq = 0; qq < p.R; ++qq) {
-                        uint32_t v[32];  // 64 bf16
-                        if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
-                        read_row_sw128(sP + ps * kSubBytes, row, v);
-                        ptx::mbar_arrive(&pempty[ps]);
-                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
-                        if (qq == 0) {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                acc[2 * e] = __uint_as_float(v[e] << 16);
-                                acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 32; ++e) {
-                                acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
-                                acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) outw[e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
                 }
                 const int sb = 0;  // one staging buffer: lane 0 issues and waits for its stores
                 if (lead && lane == 0) ptx::bulk_wait_read0();
