@@ -730,24 +730,27 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
-        if (lane == 0) {
-            const uint64_t pol = ptx::policy_evict_normal();
-            int stage = 0;
-            uint32_t ph = 0;
-            uint32_t issued = 0, issued_ph = 0;
-            bool aborted = false;
-            uint64_t w_empty = 0;
-            for (int i = 0;; ++i) {
-                if (i * G2 >= p.num_pair_units) break;
-                const int u = i * G2 + (cl + i) % G2;
-                if (u >= p.num_pair_units) continue;
-                const PUnit U = decode_pair(p, MODE, u, (int)q);
-                if (U.pad) continue;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar_prof(&empty[stage], ph ^ 1u, abort_flag, p, 10, u, w_empty)) {
-                        aborted = true;
-                        break;
-                    }
+        // The whole warp runs the loop (uniform operands); one elected lane issues.
+        const bool issuer = ptx::elect_one();
+        const uint64_t pol = ptx::policy_evict_normal();
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t issued = 0, issued_ph = 0;
+        bool aborted = false;
+        uint64_t w_empty = 0;
+        for (int i = 0;; ++i) {
+            if (i * G2 >= p.num_pair_units) break;
+            const int u = i * G2 + (cl + i) % G2;
+            if (u >= p.num_pair_units) continue;
+            const PUnit U = decode_pair(p, MODE, u, (int)q);
+            if (U.pad) continue;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const bool ok = wait_bar_prof(&empty[stage], ph ^ 1u, abort_flag, p, 10, u, w_empty);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    aborted = true;
+                    break;
+                }
+                if (issuer) {
                     // both CTAs' copies complete on the leader's full barrier
                     const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
                     if (q == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageTx2);
@@ -756,31 +759,43 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     for (int h = 0; h < 2; ++h)
                         ptx::tma_load_2d_pair(sB + stage * kBHalfBytes + h * 8192, &p.tmB[U.r], fb,
                                               U.tn * kBN + (int)q * 128 + h * 64, kb * kBK, pol);
-                    issued |= 1u << stage;
-                    issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
-                    if (++stage == kStages2) { stage = 0; ph ^= 1u; }
                 }
-                if (aborted) break;
+                __syncwarp();
+                issued |= 1u << stage;
+                issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
+                if (++stage == kStages2) { stage = 0; ph ^= 1u; }
             }
+            if (aborted) break;
+        }
+        if (lane == 0) {
             prof_add(p, 1, w_empty);
             prof_add(p, 8, 1);
-            if (q == 0) {
-                for (int s = 0; s < kStages2; ++s)
-                    if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
-            } else if (aborted) {
-                // this CTA's copies land on the leader's barriers: give them time to land
-                const uint64_t t0 = ptx::globaltimer();
-                while (ptx::globaltimer() - t0 < 50000) {}
-            }
+        }
+        if (q == 0) {
+            for (int s = 0; s < kStages2; ++s)
+                if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
+        } else if (aborted) {
+            // this CTA's copies land on the leader's barriers: give them time to land
+            const uint64_t t0 = ptx::globaltimer();
+            while (ptx::globaltimer() - t0 < 50000) {}
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader only)
-        if (lane == 0 && q == 0) {
+        // The whole warp runs the loop, so the descriptors are warp-uniform values;
+        // one elected lane issues every MMA and every commit (a commit tracks the
+        // MMAs of the thread that issues it).  Issuing from a diverged single lane
+        // measured ~70 cycles per MMA against ~45 here, and commit arrivals queue
+        // behind MMA issue, so the cheaper issue is what keeps the tensor pipe fed.
+        if (q == 0) {
+            const bool issuer = ptx::elect_one();  // the same lane issues every MMA and commit
             int stage = 0;
             uint32_t ph = 0;
             int it = 0;
             uint64_t w_full = 0, w_tempty = 0;
             const uint64_t c_start = clock64();
+            // descriptor of stage 0; stage s adds s * stage bytes / 16 to the start-address field
+            const uint64_t adesc0 = sdesc(ptx::smem_u32(sA), 16, 1024);
+            const uint64_t bdesc0 = sdesc(ptx::smem_u32(sB), 8192, 1024);
             for (int i = 0;; ++i) {
                 if (i * G2 >= p.num_pair_units) break;
                 const int u = i * G2 + (cl + i) % G2;
@@ -788,31 +803,39 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (decode_pair(p, MODE, u, 0).pad) continue;
                 const int buf = it % kAccBufs2;
                 const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
-                if (!wait_bar_prof(&tempty[buf], tph ^ 1u, abort_flag, p, 11, u, w_tempty)) break;
+                const bool tok = wait_bar_prof(&tempty[buf], tph ^ 1u, abort_flag, p, 11, u, w_tempty);
+                if (!__all_sync(0xFFFFFFFFu, tok)) break;
                 ptx::tc_fence_after();
                 const uint32_t d = tmem_base + buf * kBN;
                 bool ok = true;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar_prof(&full[stage], ph, abort_flag, p, 12, u, w_full)) { ok = false; break; }
+                    const bool fok = wait_bar_prof(&full[stage], ph, abort_flag, p, 12, u, w_full);
+                    if (!__all_sync(0xFFFFFFFFu, fok)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t a0 = ptx::smem_u32(sA + stage * kAHalfBytes);
-                    const uint32_t b0 = ptx::smem_u32(sB + stage * kBHalfBytes);
+                    const uint64_t ad = adesc0 + (uint64_t)(stage * (kAHalfBytes >> 4));
+                    const uint64_t bd = bdesc0 + (uint64_t)(stage * (kBHalfBytes >> 4));
+                    if (issuer) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        ptx::umma_bf16_pair(d, sdesc(a0 + kk * 32, 16, 1024), sdesc(b0 + kk * 2048, 8192, 1024),
-                                            kIdesc2, (kb | kk) != 0);
-                    ptx::umma_commit_pair_multicast(&empty[stage], 0x3);
+                        for (int kk = 0; kk < kBK / 16; ++kk)  // K16 steps: +32 bytes in A's rows, +16 rows of B
+                            ptx::umma_bf16_pair(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128), kIdesc2,
+                                                (kb | kk) != 0);
+                        ptx::umma_commit_pair_multicast(&empty[stage], 0x3);
+                        if (kb == p.num_kb - 1) ptx::umma_commit_pair_multicast(&tfull[buf], 0x3);
+                    }
+                    __syncwarp();
                     if (++stage == kStages2) { stage = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                ptx::umma_commit_pair_multicast(&tfull[buf], 0x3);
                 ++it;
             }
-            ptx::umma_commit_pair(mma_done);
+            if (issuer) ptx::umma_commit_pair(mma_done);
+            __syncwarp();
             drain_bar(mma_done, 0, p);
-            prof_add(p, 2, w_full);
-            prof_add(p, 3, w_tempty);
-            prof_add(p, 4, (uint64_t)(clock64() - c_start));
+            if (lane == 0) {
+                prof_add(p, 2, w_full);
+                prof_add(p, 3, w_tempty);
+                prof_add(p, 4, (uint64_t)(clock64() - c_start));
+            }
         }
     } else if (warp == 2) {
         // ------------------------------------------------------------ partial loader (own tile)
