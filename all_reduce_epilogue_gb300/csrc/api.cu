@@ -169,8 +169,10 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         if (e == cudaSuccess && mode == kModeRS)
             e = make_tmap_bf16(&p->tmOut[r], out[r], (uint64_t)N, (uint64_t)S, 64, (uint32_t)H);
     }
-    for (int v = 0; v < nviews && e == cudaSuccess; ++v)
+    for (int v = 0; v < nviews && e == cudaSuccess; ++v) {
         e = make_tmap_bf16(&p->tmOut[v], views[v], (uint64_t)N, (uint64_t)M, 64, kBM);
+        p->views[v] = const_cast<are_bf16*>(views[v]);
+    }
     if (e != cudaSuccess) {
         delete p;
         return ARE_EINVAL;

@@ -86,6 +86,7 @@ struct GemmParams {
     CUtensorMap tmA[kMaxRanks];
     CUtensorMap tmB[kMaxRanks];
     CUtensorMap tmOut[kMaxRanks];
+    are_bf16* views[kMaxRanks];  // GEMM+AR: distinct output views (the pair kernel stores with st.global)
     uint8_t* part;       // [R][T][tile part bytes]
     uint32_t* mask;      // [T]
     DevStatus* status;

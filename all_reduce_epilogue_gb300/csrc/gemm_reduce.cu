@@ -92,12 +92,15 @@ __device__ __forceinline__ int unit_of(int b, int i, int G) { return i * G + (b 
 
 // Bounded wait on an mbarrier phase; gives up when the CTA aborts or the
 // workspace timeout expires (recording the error).
+// Roles off the MMA's critical path pass a back-off so that their polling
+// leaves the SM's issue slots to the producer and MMA warps.
 __device__ __noinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                      const GemmParams& p, int id, int unit) {
+                                      const GemmParams& p, int id, int unit, uint32_t backoff_ns = 0) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer();
     while (true) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (backoff_ns) ptx::nanosleep(backoff_ns);
         if (*abort_flag) return false;
         if (ptx::globaltimer() - t0 > p.timeout_ns) {
             record_error(p.status, ARE_DEV_PIPE_TIMEOUT, blockIdx.x, id, unit);
@@ -119,10 +122,11 @@ __device__ __noinline__ void drain_bar(uint64_t* bar, uint32_t parity, const Gem
 // wait_bar that, under ARE_DEBUG_WAIT_PROFILE, adds the SM cycles spent
 // waiting to `acc`.
 __device__ __forceinline__ bool wait_bar_prof(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                              const GemmParams& p, int id, int unit, uint64_t& acc) {
-    if (!(p.flags & ARE_DEBUG_WAIT_PROFILE)) return wait_bar(bar, parity, abort_flag, p, id, unit);
+                                              const GemmParams& p, int id, int unit, uint64_t& acc,
+                                              uint32_t backoff_ns = 0) {
+    if (!(p.flags & ARE_DEBUG_WAIT_PROFILE)) return wait_bar(bar, parity, abort_flag, p, id, unit, backoff_ns);
     const uint64_t t0 = clock64();
-    const bool ok = wait_bar(bar, parity, abort_flag, p, id, unit);
+    const bool ok = wait_bar(bar, parity, abort_flag, p, id, unit, backoff_ns);
     acc += (uint64_t)(clock64() - t0);
     return ok;
 }
@@ -912,7 +916,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             if (U.pad) continue;
             const int buf = it % kAccBufs2;
             const uint32_t tph = (uint32_t)(it / kAccBufs2) & 1u;
-            if (!wait_bar_prof(&tfull[buf], tph, abort_flag, p, 14, u, w_tfull)) bad = true;
+            if (!wait_bar_prof(&tfull[buf], tph, abort_flag, p, 14, u, w_tfull, 200)) bad = true;
             if (grp_bar_or<1>(bad)) { bad = true; break; }
             ptx::tc_fence_after();
             const uint32_t tacc = tmem_base + lane_base + buf * kBN;
@@ -998,7 +1002,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         float acc[16];
                         for (int qq = 0; qq < p.R; ++qq) {
                             uint32_t v[16];
-                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
+                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
                             read_row_sw64(sP + ps * kPSub2, row, v);
                             ptx::mbar_arrive(&pempty[ps]);
                             if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
@@ -1019,7 +1023,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         float acc[32];
                         for (int qq = 0; qq < p.R; ++qq) {
                             uint32_t v[16];  // 32 bf16
-                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull)) bad = true;
+                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
                             read_row_sw64(sP + ps * kPSub2, row, v);
                             ptx::mbar_arrive(&pempty[ps]);
                             if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
@@ -1042,9 +1046,35 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     }
                 }
                 const int sb = 0;  // one staging buffer: lane 0 issues and waits for its stores
-                if (lead && lane == 0) ptx::bulk_wait_read0();
+                if (MODE == kModeRS && lead && lane == 0) ptx::bulk_wait_read0();
                 if (grp_bar_or<2>(bad)) { bad = true; break; }
                 write_row_sw128(sOut, row, outw);
+                if (MODE == kModeAR) {
+                    // every view gets the chunk through coalesced 16-byte stores: thread t moves
+                    // 16-byte column chunk t mod 8 of rows t/8 + 16i, so a warp writes four whole
+                    // 128-byte row segments per store.  The TMA engine stays free for the
+                    // mainloop's operand loads (R views of TMA stores measured 17% slower).
+                    grp_bar<2>();
+                    const int x = U.tn * kBN + c * 64;
+                    const int cc = row & 7;
+                    const int gcol = x + cc * 8;
+                    uint4 v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = (row >> 3) + 16 * i;
+                        v[i] = *reinterpret_cast<const uint4*>(sOut + r * 128 + ((cc ^ (r & 7)) << 4));
+                    }
+                    if (gcol < p.N) {
+                        for (int w = 0; w < p.nviews; ++w) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int grow = row0 + (row >> 3) + 16 * i;
+                                if (grow < p.M) ptx::st_stream_v4(p.views[w] + (size_t)grow * p.N + gcol, v[i]);
+                            }
+                        }
+                    }
+                    continue;  // the next chunk's barrier orders these reads before sOut is rewritten
+                }
                 ptx::fence_proxy_async_shared();
                 grp_bar<2>();
                 if (lead && lane == 0) {
