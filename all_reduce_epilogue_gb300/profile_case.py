@@ -25,6 +25,7 @@ def main(argv=None) -> int:
     ap.add_argument("--N", type=int, default=7168)
     ap.add_argument("--K", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--views", type=int, default=0, help="gemm_ar: distinct output views (default R)")
     ap.add_argument("--seed", type=int, default=0)
     a = ap.parse_args(argv)
     torch.manual_seed(a.seed)
@@ -52,7 +53,9 @@ def main(argv=None) -> int:
                 for _ in range(a.iters):
                     are.gemm_rs(A, B, out, ws)
             else:
-                views = [torch.empty(a.M, a.N, dtype=torch.bfloat16, device=dev) for _ in range(a.R)]
+                nv = a.views if a.views > 0 else a.R
+                distinct = [torch.empty(a.M, a.N, dtype=torch.bfloat16, device=dev) for _ in range(nv)]
+                views = [distinct[r % nv] for r in range(a.R)]
                 for _ in range(a.iters):
                     are.gemm_ar(A, B, views, ws)
             st = ws.device_status()
