@@ -198,10 +198,18 @@ __device__ __forceinline__ int consumed_row(int G) {
     return i < 0 ? i + G : i;
 }
 
+// ARE_DEBUG_WAIT_PROFILE: one thread of each role adds the SM cycles it spent
+// waiting to the debug counters.
+__device__ __forceinline__ bool prof_on(const ArParams& p) { return (p.flags & ARE_DEBUG_WAIT_PROFILE) != 0; }
+__device__ __forceinline__ void prof_add(const ArParams& p, int slot, uint64_t v) {
+    if (prof_on(p) && v) atomicAdd(&p.counters[slot], (unsigned long long)v);
+}
+
 // ------------------------------------------------------------------ phase B
 template <int PPT>
 __device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, int64_t row, uint32_t* srow, int bt,
-                                         const uint8_t* res_smem, uint64_t keep, uint32_t sent, uint32_t rearm) {
+                                         const uint8_t* res_smem, uint64_t keep, uint32_t sent, uint32_t rearm,
+                                         uint64_t& w_spin) {
     const int P = p.packs_per_row;
     uint4 lo[PPT], hi[PPT], res[PPT];
 #pragma unroll
@@ -218,6 +226,7 @@ __device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, in
     for (int k = 0; k < PPT; ++k) {
         const int pk = bt + k * kBThreads;
         if (pk < P && (has_word(lo[k], sent) || has_word(hi[k], sent))) {
+            const uint64_t c0 = clock64();
             const uint64_t t0 = ptx::globaltimer();
             while (true) {
                 lo[k] = ptx::ld_relaxed_gpu_v4(srow + pk * 8);
@@ -230,6 +239,7 @@ __device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, in
                     break;
                 }
             }
+            w_spin += (uint64_t)(clock64() - c0);
         }
     }
     // Re-arm every pack this thread consumed (it is the pack's only consumer).
@@ -334,10 +344,13 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
             uint32_t ph = 0, rph = 0;
             uint32_t issued = 0, issued_ph = 0, rissued = 0, rissued_ph = 0;
             bool ok = true;
+            uint64_t w_empty = 0;
             for (int c = 0; c < p.num_chunks && ok; ++c) {
                 const Slice sl = slice_of(p, c);
                 if (res_smem && consume < sl.rows) {  // residual row of this block's phase-B row
+                    const uint64_t c0 = clock64();
                     if (!ar_wait(&sh.rempty[rs], rph ^ 1u, sh, p)) break;
+                    w_empty += (uint64_t)(clock64() - c0);
                     const uint32_t bytes = (uint32_t)p.N * 2;
                     ptx::mbar_arrive_expect_tx(&sh.rfull[rs], bytes);
                     const int64_t row = (int64_t)c * p.chunk_rows + consume;
@@ -349,7 +362,9 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                 }
                 for (int64_t q = sl.q0; q < sl.q1; q += kAThreads) {
                     const int n = (int)min((int64_t)kAThreads, sl.q1 - q);
+                    const uint64_t c0 = clock64();
                     if (!ar_wait(&sh.empty[s], ph ^ 1u, sh, p)) { ok = false; break; }
+                    w_empty += (uint64_t)(clock64() - c0);
                     ptx::mbar_arrive_expect_tx(&sh.full[s], (uint32_t)(p.R * n * 16));
                     for (int r = 0; r < p.R; ++r)
                         ptx::bulk_load_hint(sh.stage + (size_t)s * kStageBytes + r * kRankBytes,
@@ -359,6 +374,8 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                     if (++s == p.stages) { s = 0; ph ^= 1u; }
                 }
             }
+            prof_add(p, 1, w_empty);
+            prof_add(p, 8, 1);
             // every bulk copy issued must land before the block exits
             for (int i = 0; i < p.stages; ++i) {
                 if (issued & (1u << i)) {
@@ -382,8 +399,10 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
         int s = 0;
         uint32_t ph = 0;
         uint32_t ncanon = 0;
+        uint64_t w_full = 0, w_ahead = 0, w_ring = 0;
         for (int c = 0; c < p.num_chunks; ++c) {
             if (c >= kAhead) {  // stay at most kAhead chunks ahead of this block's phase B
+                const uint64_t c0 = clock64();
                 const uint64_t t0 = ptx::globaltimer();
                 while (*sh.bdone < c - kAhead + 1) {
                     if (*sh.abort) break;
@@ -393,6 +412,7 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                         break;
                     }
                 }
+                w_ahead += (uint64_t)(clock64() - c0);
             }
             const Slice sl = slice_of(p, c);
             uint32_t* chunk_staging = staging_row(p, c, 0);
@@ -408,8 +428,11 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                     chk0 = ptx::ld_relaxed_gpu_v4(dst);
                     chk1 = ptx::ld_relaxed_gpu_v4(dst + 4);
                 }
+                uint64_t c0 = clock64();
                 const bool ready = ar_wait(&sh.full[s], ph, sh, p);
+                w_full += (uint64_t)(clock64() - c0);
                 if (lap > 0 && at < n && !(all_words(chk0, sent) && all_words(chk1, sent))) {
+                    c0 = clock64();
                     const uint64_t t0 = ptx::globaltimer();
                     while (true) {
                         chk0 = ptx::ld_relaxed_gpu_v4(dst);
@@ -422,6 +445,7 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                             break;
                         }
                     }
+                    w_ring += (uint64_t)(clock64() - c0);
                 }
                 if (ready && at < n) {
                     const uint8_t* src = sh.stage + (size_t)s * kStageBytes + at * 16;
@@ -456,6 +480,11 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                 if (++s == p.stages) { s = 0; ph ^= 1u; }
             }
         }
+        if (at == 0) {
+            prof_add(p, 2, w_full);
+            prof_add(p, 3, w_ahead);
+            prof_add(p, 4, w_ring);
+        }
         if (p.flags & ARE_DEBUG_COUNT_CANON) {
             uint32_t cnt = ncanon;
 #pragma unroll
@@ -468,23 +497,32 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
         const uint64_t keep = ptx::policy_evict_last();
         int rs = 0;
         uint32_t rph = 0;
+        uint64_t w_spin = 0, w_res = 0;
+        const uint64_t c_start = clock64();
         for (int c = 0; c < p.num_chunks; ++c) {
             const int64_t row0 = (int64_t)c * p.chunk_rows;
             const int rows = (int)min((int64_t)p.chunk_rows, (int64_t)p.M - row0);
             if (consume < rows) {
                 const uint8_t* res_src = nullptr;
                 if (res_smem) {
+                    const uint64_t c0 = clock64();
                     ar_wait(&sh.rfull[rs], rph, sh, p);
+                    w_res += (uint64_t)(clock64() - c0);
                     res_src = sh.res + (size_t)rs * p.N * 2;
                 }
                 norm_row<PPT>(p, sh, row0 + consume, staging_row(p, c, consume), bt, res_src, keep,
-                              sentinel_of(lap_of(p, c)), rearm_value(p, c, consume));
+                              sentinel_of(lap_of(p, c)), rearm_value(p, c, consume), w_spin);
                 if (res_smem) {
                     ptx::mbar_arrive(&sh.rempty[rs]);
                     if (++rs == kResSlots) { rs = 0; rph ^= 1u; }
                 }
             }
             if (bt == 0) *sh.bdone = c + 1;
+        }
+        if (bt == 0) {
+            prof_add(p, 5, w_spin);
+            prof_add(p, 6, w_res);
+            prof_add(p, 7, (uint64_t)(clock64() - c_start));
         }
     }
 }

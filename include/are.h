@@ -105,7 +105,8 @@ enum {
     ARE_DEBUG_SKIP_PUBLISH = 8u,  /* GEMM: work unit `debug_arg` never sets its ready bit */
     ARE_DEBUG_SKIP_STAGE = 16u,   /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
     ARE_DEBUG_SINGLE_CTA = 32u,   /* GEMM: use the one-CTA kernel even where the CTA-pair kernel applies */
-    ARE_DEBUG_WAIT_PROFILE = 64u  /* GEMM (CTA-pair kernel): add each role's waiting SM cycles to the counters */
+    ARE_DEBUG_WAIT_PROFILE = 64u  /* GEMM (CTA-pair kernel) and AR+RMSNorm: add each role's waiting SM cycles
+                                     to the counters (see ARE_SNAP_COUNTERS) */
 };
 
 /* Device status word, see are_get_device_status(). */
@@ -133,7 +134,11 @@ enum {
                               waiting for operands, [3] MMA waiting for a free accumulator, [4] MMA thread
                               from its first wait to its last commit, [5] drain waiting for an accumulator,
                               [6] loader waiting for tile masks, [7] reduce waiting for partial sub-tiles,
-                              [8] CTAs counted */
+                              [8] CTAs counted.  For AR+RMSNorm: [1] producer waiting for a free stage or
+                              residual slot, [2] phase A waiting for partials, [3] phase A held back by
+                              its own phase B, [4] phase A waiting for a ring slot's re-arm, [5] phase B
+                              spinning on staged words, [6] phase B waiting for its residual row, [7]
+                              phase B span, [8] blocks counted */
 };
 
 typedef struct are_ws are_ws;
