@@ -323,11 +323,11 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             ptx::mbar_init(&sh.full[s], 1);
-            ptx::mbar_init(&sh.empty[s], kAThreads);
+            ptx::mbar_init(&sh.empty[s], kAThreads / 32);  // one arrival per phase-A warp
         }
         for (int s = 0; s < kResSlots; ++s) {
             ptx::mbar_init(&sh.rfull[s], 1);
-            ptx::mbar_init(&sh.rempty[s], kBThreads);
+            ptx::mbar_init(&sh.rempty[s], kBThreads / 32);  // one arrival per phase-B warp
         }
         *sh.bdone = 0;
         *sh.abort = 0u;
@@ -431,6 +431,36 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                 uint64_t c0 = clock64();
                 const bool ready = ar_wait(&sh.full[s], ph, sh, p);
                 w_full += (uint64_t)(clock64() - c0);
+                const bool work = ready && at < n;
+                uint32_t wv[8];
+                if (work) {
+                    const uint8_t* src = sh.stage + (size_t)s * kStageBytes + at * 16;
+                    float acc[8];
+                    unpack8(*reinterpret_cast<const uint4*>(src), acc);
+#pragma unroll
+                    for (int r = 1; r < kMaxRanks; ++r) {
+                        if (r < p.R) {
+                            float f[8];
+                            unpack8(*reinterpret_cast<const uint4*>(src + r * kRankBytes), f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) acc[i] = acc[i] + f[i];
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        wv[i] = __float_as_uint(acc[i]);
+                        if (wv[i] == kSentinelF32) {  // producer-side canonicalisation
+                            wv[i] = 0u;
+                            ++ncanon;
+                        }
+                        if (acc[i] != acc[i]) wv[i] = kCanonicalNaN;  // never a ring sentinel
+                    }
+                }
+                // the warp's reads of the stage are done: one lane releases it
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sh.empty[s]);
+                // the ring check, loaded before the wait, is verified only now, so its L2
+                // round trip overlaps the wait and the sums; the pack is written after it
                 if (lap > 0 && at < n && !(all_words(chk0, sent) && all_words(chk1, sent))) {
                     c0 = clock64();
                     const uint64_t t0 = ptx::globaltimer();
@@ -447,36 +477,13 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                     }
                     w_ring += (uint64_t)(clock64() - c0);
                 }
-                if (ready && at < n) {
-                    const uint8_t* src = sh.stage + (size_t)s * kStageBytes + at * 16;
-                    float acc[8];
-                    unpack8(*reinterpret_cast<const uint4*>(src), acc);
-#pragma unroll
-                    for (int r = 1; r < kMaxRanks; ++r) {
-                        if (r < p.R) {
-                            float f[8];
-                            unpack8(*reinterpret_cast<const uint4*>(src + r * kRankBytes), f);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) acc[i] = acc[i] + f[i];
-                        }
-                    }
-                    uint32_t wv[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        wv[i] = __float_as_uint(acc[i]);
-                        if (wv[i] == kSentinelF32) {  // producer-side canonicalisation
-                            wv[i] = 0u;
-                            ++ncanon;
-                        }
-                        if (acc[i] != acc[i]) wv[i] = kCanonicalNaN;  // never a ring sentinel
-                    }
+                if (work) {
                     const int64_t pack = sl.base + q + at;
                     if (!((p.flags & ARE_DEBUG_SKIP_STAGE) && pack == p.debug_arg)) {
                         ptx::st_v4_hint(dst, make_uint4(wv[0], wv[1], wv[2], wv[3]), keep);
                         ptx::st_v4_hint(dst + 4, make_uint4(wv[4], wv[5], wv[6], wv[7]), keep);
                     }
                 }
-                ptx::mbar_arrive(&sh.empty[s]);
                 if (++s == p.stages) { s = 0; ph ^= 1u; }
             }
         }
@@ -513,7 +520,8 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
                 norm_row<PPT>(p, sh, row0 + consume, staging_row(p, c, consume), bt, res_src, keep,
                               sentinel_of(lap_of(p, c)), rearm_value(p, c, consume), w_spin);
                 if (res_smem) {
-                    ptx::mbar_arrive(&sh.rempty[rs]);
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&sh.rempty[rs]);
                     if (++rs == kResSlots) { rs = 0; rph ^= 1u; }
                 }
             }
