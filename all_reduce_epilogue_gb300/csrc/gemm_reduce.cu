@@ -225,70 +225,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol = ptx::policy_evict_normal();
-            int stage = 0;
-            uint32_t ph = 0;
-            uint32_t issued = 0, issued_ph = 0;  // bit s: stage s has a fill in flight; its parity
-            for (int i = 0;; ++i) {
-                if (i * G >= p.num_units) break;
-                const int u = unit_of(b, i, G);
-                if (u >= p.num_units) continue;
-                const Unit U = decode(p, MODE, u);
-                bool ok = true;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(&empty[stage], ph ^ 1u, abort_flag, p, 0, u)) { ok = false; break; }
+        // The whole warp runs the loop; one elected lane issues (see the pair kernel).
+        const bool issuer = ptx::elect_one();
+        const uint64_t pol = ptx::policy_evict_normal();
+        int stage = 0;
+        uint32_t ph = 0;
+        uint32_t issued = 0, issued_ph = 0;  // bit s: stage s has a fill in flight; its parity
+        for (int i = 0;; ++i) {
+            if (i * G >= p.num_units) break;
+            const int u = unit_of(b, i, G);
+            if (u >= p.num_units) continue;
+            const Unit U = decode(p, MODE, u);
+            bool ok = true;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const bool eok = wait_bar(&empty[stage], ph ^ 1u, abort_flag, p, 0, u);
+                if (!__all_sync(0xFFFFFFFFu, eok)) { ok = false; break; }
+                if (issuer) {
                     ptx::mbar_arrive_expect_tx(&full[stage], kStageTx);
-                    ptx::tma_load_2d(sA + stage * kAStageBytes, &p.tmA[U.r], &full[stage], kb * kBK, U.tm * kBM, pol);
+                    ptx::tma_load_2d(sA + stage * kAStageBytes, &p.tmA[U.r], &full[stage], kb * kBK, U.tm * kBM,
+                                     pol);
 #pragma unroll
                     for (int q = 0; q < kBN / 64; ++q)
                         ptx::tma_load_2d(sB + stage * kBStageBytes + q * 8192, &p.tmB[U.r], &full[stage],
                                          U.tn * kBN + q * 64, kb * kBK, pol);
-                    issued |= 1u << stage;
-                    issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
-                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
                 }
-                if (!ok) break;
+                __syncwarp();
+                issued |= 1u << stage;
+                issued_ph = (issued_ph & ~(1u << stage)) | (ph << stage);
+                if (++stage == kStages) { stage = 0; ph ^= 1u; }
             }
-            for (int s = 0; s < kStages; ++s)
-                if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
+            if (!ok) break;
         }
+        for (int s = 0; s < kStages; ++s)
+            if (issued & (1u << s)) drain_bar(&full[s], (issued_ph >> s) & 1u, p);
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t ph = 0;
-            int it = 0;
-            for (int i = 0;; ++i) {
-                if (i * G >= p.num_units) break;
-                const int u = unit_of(b, i, G);
-                if (u >= p.num_units) continue;
-                const int buf = it & 1;
-                const uint32_t tph = (it >> 1) & 1;
-                if (!wait_bar(&tempty[buf], tph ^ 1u, abort_flag, p, 1, u)) break;
+        // The whole warp runs the loop with warp-uniform descriptors; one elected
+        // lane issues every MMA and every commit.
+        const bool issuer = ptx::elect_one();
+        int stage = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        const uint64_t adesc0 = sdesc(ptx::smem_u32(sA), 16, 1024);
+        const uint64_t bdesc0 = sdesc(ptx::smem_u32(sB), 8192, 1024);
+        for (int i = 0;; ++i) {
+            if (i * G >= p.num_units) break;
+            const int u = unit_of(b, i, G);
+            if (u >= p.num_units) continue;
+            const int buf = it & 1;
+            const uint32_t tph = (it >> 1) & 1;
+            const bool tok = wait_bar(&tempty[buf], tph ^ 1u, abort_flag, p, 1, u);
+            if (!__all_sync(0xFFFFFFFFu, tok)) break;
+            ptx::tc_fence_after();
+            const uint32_t d = tmem_base + buf * kBN;
+            bool ok = true;
+            for (int kb = 0; kb < p.num_kb; ++kb) {
+                const bool fok = wait_bar(&full[stage], ph, abort_flag, p, 2, u);
+                if (!__all_sync(0xFFFFFFFFu, fok)) { ok = false; break; }
                 ptx::tc_fence_after();
-                const uint32_t d = tmem_base + buf * kBN;
-                bool ok = true;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!wait_bar(&full[stage], ph, abort_flag, p, 2, u)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    const uint32_t a0 = ptx::smem_u32(sA + stage * kAStageBytes);
-                    const uint32_t b0 = ptx::smem_u32(sB + stage * kBStageBytes);
+                const uint64_t ad = adesc0 + (uint64_t)(stage * (kAStageBytes >> 4));
+                const uint64_t bd = bdesc0 + (uint64_t)(stage * (kBStageBytes >> 4));
+                if (issuer) {
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        ptx::umma_bf16(d, sdesc(a0 + kk * 32, 16, 1024), sdesc(b0 + kk * 2048, 8192, 1024), kIdesc,
-                                       (kb | kk) != 0);
+                    for (int kk = 0; kk < kBK / 16; ++kk)  // K16 steps: +32 bytes in A's rows, +16 rows of B
+                        ptx::umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 128), kIdesc, (kb | kk) != 0);
                     ptx::umma_commit(&empty[stage]);
-                    if (++stage == kStages) { stage = 0; ph ^= 1u; }
+                    if (kb == p.num_kb - 1) ptx::umma_commit(&tfull[buf]);
                 }
-                if (!ok) break;
-                ptx::umma_commit(&tfull[buf]);
-                ++it;
+                __syncwarp();
+                if (++stage == kStages) { stage = 0; ph ^= 1u; }
             }
-            // every MMA this thread issued has completed once mma_done flips
-            ptx::umma_commit(mma_done);
-            drain_bar(mma_done, 0, p);
+            if (!ok) break;
+            ++it;
         }
+        // every MMA the issuing lane issued has completed once mma_done flips
+        if (issuer) ptx::umma_commit(mma_done);
+        __syncwarp();
+        drain_bar(mma_done, 0, p);
     } else if (warp == 2) {
         // ------------------------------------------------------------ partial loader
         if (lane == 0) {
