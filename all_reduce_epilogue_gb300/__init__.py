@@ -29,7 +29,7 @@ OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBUSY, ENODEV, ECAPACITY = range(8)
 OP_GEMM_RS, OP_GEMM_AR, OP_ALLREDUCE_RMSNORM = 1, 2, 3
 # debug flags
 DEBUG_NO_REARM, DEBUG_LOG_PIECES, DEBUG_COUNT_CANON, DEBUG_SKIP_PUBLISH, DEBUG_SKIP_STAGE = 1, 2, 4, 8, 16
-DEBUG_SINGLE_CTA, DEBUG_WAIT_PROFILE = 32, 64
+DEBUG_SINGLE_CTA, DEBUG_WAIT_PROFILE, DEBUG_AR_ONESHOT, DEBUG_AR_LAMPORT = 32, 64, 128, 256
 # device status codes
 DEV_OK, DEV_MASK_TIMEOUT, DEV_STAGE_TIMEOUT, DEV_PIPE_TIMEOUT = 0, 1, 2, 3
 # snapshot kinds
@@ -40,7 +40,8 @@ TILE_M, TILE_N = 128, 256
 # Every C-ABI symbol declared in include/are.h.
 EXPORTS = [
     "are_version", "are_status_string", "are_supports", "are_workspace_create", "are_workspace_destroy",
-    "are_workspace_reset", "are_workspace_set_debug", "are_get_device_status", "are_debug_snapshot",
+    "are_workspace_reset", "are_workspace_set_debug", "are_workspace_set_oneshot_max_bytes",
+    "are_get_device_status", "are_debug_snapshot",
     "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_rmsnorm_noalloc",
 ]
 
@@ -92,6 +93,8 @@ def load_library(path: str = LIB_PATH):
     lib.are_workspace_reset.argtypes = [vp]
     lib.are_workspace_set_debug.restype = i32
     lib.are_workspace_set_debug.argtypes = [vp, u32, i64]
+    lib.are_workspace_set_oneshot_max_bytes.restype = i32
+    lib.are_workspace_set_oneshot_max_bytes.argtypes = [vp, u64]
     lib.are_get_device_status.restype = i32
     lib.are_get_device_status.argtypes = [vp, ctypes.POINTER(_DevStatus)]
     lib.are_debug_snapshot.restype = i32
@@ -187,6 +190,12 @@ class Workspace:
 
     def set_debug(self, flags: int, arg: int = -1):
         _check(load_library().are_workspace_set_debug(self.handle, flags, arg), "are_workspace_set_debug")
+
+    def set_oneshot_max_bytes(self, nbytes: int):
+        """Per-rank input size (M*N*2 bytes) up to which allreduce_rmsnorm uses
+        its one-shot kernel (0: always the Lamport kernel)."""
+        _check(load_library().are_workspace_set_oneshot_max_bytes(self.handle, nbytes),
+               "are_workspace_set_oneshot_max_bytes")
 
     def device_status(self) -> dict:
         st = _DevStatus()

@@ -36,6 +36,7 @@ struct are_ws {
     uint32_t* d_staging = nullptr;
     size_t staging_words = 0;
     int ar_resident[kArMaxPpt + 1] = {0};
+    uint64_t oneshot_max_bytes = 0;   // set at creation
     std::mutex mu;
     uint32_t debug_flags = 0;
     int64_t debug_arg = -1;
@@ -46,6 +47,9 @@ struct are_ws {
 namespace {
 
 constexpr uint64_t kDefaultTimeoutNs = 200ull * 1000 * 1000;
+// AR+RMSNorm: per-rank input bytes (M * N * 2) at or below which the one-shot
+// kernel runs instead of the Lamport kernel.
+constexpr uint64_t kOneShotMaxBytes = 448ull * 1024;
 constexpr size_t kCounterWords = 16;
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -284,6 +288,7 @@ are_status are_workspace_create(are_ws** out, const are_caps* caps) {
     ws->num_sms = prop.multiProcessorCount;
     ws->caps = *caps;
     ws->debug_flags = caps->debug_flags;
+    ws->oneshot_max_bytes = kOneShotMaxBytes;
     ws->timeout_ns = caps->timeout_ns ? caps->timeout_ns : kDefaultTimeoutNs;
 
     e = cudaMalloc(&ws->d_status, sizeof(DevStatus));
@@ -304,6 +309,7 @@ are_status are_workspace_create(are_ws** out, const are_caps* caps) {
     }
     if (e == cudaSuccess) {
         for (int ppt = 1; ppt <= kArMaxPpt; ++ppt) ws->ar_resident[ppt] = ar_rmsnorm_resident_blocks(ppt, ws->num_sms);
+        if (e == cudaSuccess) e = ar_oneshot_prepare();
     }
     if (e != cudaSuccess) {
         are_status st = from_cuda(e);
@@ -341,6 +347,14 @@ are_status are_workspace_set_debug(are_ws* ws, uint32_t flags, int64_t arg) {
     if (!lk.ok) return ARE_EBUSY;
     ws->debug_flags = flags;
     ws->debug_arg = arg;
+    return ARE_OK;
+}
+
+are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t bytes) {
+    if (!ws) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    ws->oneshot_max_bytes = bytes;
     return ARE_OK;
 }
 
@@ -429,7 +443,17 @@ are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf1
     p.timeout_ns = ws->timeout_ns;
     ws->last_ar_M = M;
     ws->last_ar_N = N;
-    return from_cuda(launch_ar_rmsnorm(p, ppt, grid, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Small messages take the one-shot kernel (no staging), larger ones the Lamport
+    // kernel; the threshold is a per-rank input size, as in the pages' dispatch.
+    const bool fits = ar_oneshot_fits(R, (int)N, residual != nullptr);
+    const bool oneshot = fits && !(ws->debug_flags & ARE_DEBUG_AR_LAMPORT) &&
+                         ((ws->debug_flags & ARE_DEBUG_AR_ONESHOT) || (uint64_t)M * (uint64_t)N * 2 <= ws->oneshot_max_bytes);
+    if (oneshot) {
+        const int os_grid = (int)std::min<int64_t>(M, ws->num_sms);
+        return from_cuda(launch_ar_oneshot(p, ppt, os_grid, s));
+    }
+    return from_cuda(launch_ar_rmsnorm(p, ppt, grid, s));
 }
 
 }  // extern "C"

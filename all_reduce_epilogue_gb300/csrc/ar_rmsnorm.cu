@@ -535,6 +535,127 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
     }
 }
 
+// ------------------------------------------------------------------ one-shot path
+// Small messages: ROCm/aiter PR #4977, the commits that re-baseline against the
+// one-stage kernel.  A reduce-scatter cannot beat a kernel that reads every
+// rank's input once and stages nothing when the message is small, so the fused
+// operation takes the one-shot kernel below a per-rank byte threshold set at the
+// measured crossover, and the Lamport kernel above it.
+//
+// One row per block: one thread bulk-copies the R partial rows and the residual
+// row into shared memory under one mbarrier; the 256 threads sum them in ring
+// order, canonicalise exactly as the Lamport producer does, add the residual and
+// normalise with the same per-thread pack order and block reduction as phase B,
+// so both paths return the same bits.  As soon as h is in registers the shared
+// memory is handed to the next row's copies, which then overlap this row's
+// reduction and stores.
+constexpr int kOsThreads = 256;
+
+__device__ __forceinline__ bool os_wait(uint64_t* bar, uint32_t parity, const ArParams& p) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer() - t0 > p.timeout_ns) {
+            record_error(p.status, ARE_DEV_PIPE_TIMEOUT, blockIdx.x, -4, -1);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int PPT>
+__global__ void __launch_bounds__(kOsThreads, 1) ar_oneshot_kernel(const __grid_constant__ ArParams p) {
+    extern __shared__ __align__(128) uint8_t os_smem[];
+    const int P = p.packs_per_row;
+    const uint32_t row_bytes = (uint32_t)p.N * 2u;
+    const int nrows = p.R + (p.residual ? 1 : 0);
+    uint8_t* rows = os_smem;  // partial rows 0..R-1, then the residual row
+    uint64_t* bar = reinterpret_cast<uint64_t*>(os_smem + (size_t)nrows * row_bytes);
+    float* red = reinterpret_cast<float*>(bar + 1);
+    const int bt = threadIdx.x, lane = bt & 31, w = bt >> 5;
+    if (bt == 0) {
+        ptx::mbar_init(bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    const uint64_t stream_pol = ptx::policy_evict_first();
+    auto issue = [&](int64_t row) {
+        if (bt == 0) {
+            ptx::mbar_arrive_expect_tx(bar, (uint32_t)nrows * row_bytes);
+            for (int r = 0; r < p.R; ++r)
+                ptx::bulk_load_hint(rows + (size_t)r * row_bytes, p.x[r] + row * (int64_t)p.N, row_bytes, bar,
+                                    stream_pol);
+            if (p.residual)
+                ptx::bulk_load_hint(rows + (size_t)p.R * row_bytes, p.residual + row * (int64_t)p.N, row_bytes, bar,
+                                    stream_pol);
+        }
+    };
+    uint32_t ph = 0;
+    int64_t row = blockIdx.x;
+    if (row < p.M) issue(row);
+    for (; row < p.M; row += gridDim.x) {
+        if (!os_wait(bar, ph, p)) return;  // only if a copy never lands: nothing in flight is owed then
+        ph ^= 1u;
+        float h[PPT][8];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            const int pk = bt + k * kOsThreads;
+            if (pk < P) {
+                float acc[8];
+                unpack8(*reinterpret_cast<const uint4*>(rows + pk * 16), acc);
+#pragma unroll
+                for (int r = 1; r < kMaxRanks; ++r) {
+                    if (r < p.R) {
+                        float f[8];
+                        unpack8(*reinterpret_cast<const uint4*>(rows + (size_t)r * row_bytes + pk * 16), f);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i] = acc[i] + f[i];
+                    }
+                }
+                float r8[8];
+                if (p.residual) unpack8(*reinterpret_cast<const uint4*>(rows + (size_t)p.R * row_bytes + pk * 16), r8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t wv = __float_as_uint(acc[i]);
+                    if (wv == kSentinelF32) wv = 0u;                  // the Lamport producer's canonicalisation
+                    if (acc[i] != acc[i]) wv = kCanonicalNaN;
+                    h[k][i] = p.residual ? __uint_as_float(wv) + r8[i] : __uint_as_float(wv);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ss = fmaf(h[k][i], h[k][i], ss);
+            }
+        }
+        __syncthreads();  // every read of this row's shared copies is done
+        if (row + gridDim.x < p.M) issue(row + gridDim.x);
+        ss = warp_sum(ss);
+        if (lane == 0) red[w] = ss;
+        __syncthreads();
+        if (w == 0) {
+            float v = lane < (kOsThreads / 32) ? red[lane] : 0.f;
+            v = warp_sum(v);
+            if (lane == 0) red[kOsThreads / 32] = v;
+        }
+        __syncthreads();
+        const float inv = rsqrtf(red[kOsThreads / 32] * p.inv_n + p.eps);
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            const int pk = bt + k * kOsThreads;
+            if (pk < P) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
+                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+                uint4 o;
+                o.x = pack_bf16x2(h[k][0] * inv * g0.x, h[k][1] * inv * g0.y);
+                o.y = pack_bf16x2(h[k][2] * inv * g0.z, h[k][3] * inv * g0.w);
+                o.z = pack_bf16x2(h[k][4] * inv * g1.x, h[k][5] * inv * g1.y);
+                o.w = pack_bf16x2(h[k][6] * inv * g1.z, h[k][7] * inv * g1.w);
+                ptx::st_stream_v4(p.out + row * (int64_t)p.N + pk * 8, o);
+            }
+        }
+        __syncthreads();  // red[] is rewritten by the next row
+    }
+}
+
 __global__ void fill_u32_kernel(uint32_t* dst, uint32_t v, size_t n) {
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
         dst[i] = v;
@@ -594,6 +715,35 @@ cudaError_t launch_ar_rmsnorm(const ArParams& p, int ppt, int grid, cudaStream_t
         case 4: ar_rmsnorm_kernel<4><<<grid, kArThreads, smem, stream>>>(p); break;
         case 8: ar_rmsnorm_kernel<8><<<grid, kArThreads, smem, stream>>>(p); break;
         case 16: ar_rmsnorm_kernel<16><<<grid, kArThreads, smem, stream>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+size_t ar_oneshot_smem_bytes(int R, int N, bool residual) {
+    return (size_t)(R + (residual ? 1 : 0)) * (size_t)N * 2 + 8 + 16 * 4 + 64;
+}
+
+bool ar_oneshot_fits(int R, int N, bool residual) { return ar_oneshot_smem_bytes(R, N, residual) <= kSmemLimit; }
+
+cudaError_t ar_oneshot_prepare() {
+    const int lim = (int)kSmemLimit;
+    cudaError_t e = cudaFuncSetAttribute(ar_oneshot_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ar_oneshot_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ar_oneshot_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ar_oneshot_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ar_oneshot_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    return e;
+}
+
+cudaError_t launch_ar_oneshot(const ArParams& p, int ppt, int grid, cudaStream_t stream) {
+    const size_t smem = ar_oneshot_smem_bytes(p.R, p.N, p.residual != nullptr);
+    switch (ppt) {
+        case 1: ar_oneshot_kernel<1><<<grid, kOsThreads, smem, stream>>>(p); break;
+        case 2: ar_oneshot_kernel<2><<<grid, kOsThreads, smem, stream>>>(p); break;
+        case 4: ar_oneshot_kernel<4><<<grid, kOsThreads, smem, stream>>>(p); break;
+        case 8: ar_oneshot_kernel<8><<<grid, kOsThreads, smem, stream>>>(p); break;
+        case 16: ar_oneshot_kernel<16><<<grid, kOsThreads, smem, stream>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

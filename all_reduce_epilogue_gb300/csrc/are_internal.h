@@ -66,6 +66,11 @@ void ar_rmsnorm_smem_plan(ArParams& p);
 // Largest grid that is fully co-resident for the packs-per-thread variant `ppt`.
 int ar_rmsnorm_resident_blocks(int ppt, int num_sms);
 cudaError_t launch_ar_rmsnorm(const ArParams& p, int ppt, int grid, cudaStream_t stream);
+// One-shot AR+RMSNorm for small messages (one row per block, no staging).
+size_t ar_oneshot_smem_bytes(int R, int N, bool residual);
+bool ar_oneshot_fits(int R, int N, bool residual);
+cudaError_t ar_oneshot_prepare();
+cudaError_t launch_ar_oneshot(const ArParams& p, int ppt, int grid, cudaStream_t stream);
 // Fill n 32-bit words with v.
 cudaError_t launch_fill_u32(uint32_t* dst, uint32_t v, size_t n, cudaStream_t stream);
 

@@ -356,6 +356,25 @@ def run_gpu(args):
     ms_step = max_over_ranks(dist, total_ms / args.steps, dev)
     per_ms = {p: statistics.mean(v) for p, v in per.items()}
 
+    # The one-shot AR+RMSNorm kernel on the same workload (forced; the default
+    # dispatch sends this size to the Lamport kernel).  Reported beside the
+    # step, not part of it.
+    ws.set_debug(are.DEBUG_AR_ONESHOT)
+    for _ in range(args.warmup):
+        are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
+    o0 = torch.cuda.Event(enable_timing=True)
+    o1 = torch.cuda.Event(enable_timing=True)
+    o0.record(stream)
+    for _ in range(args.steps):
+        are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
+    o1.record(stream)
+    torch.cuda.synchronize(dev)
+    ws.set_debug(0)
+    st = ws.device_status()
+    if st["code"] != 0:
+        raise RuntimeError(f"device status after one-shot steps: {st}")
+    oneshot_ms = max_over_ranks(dist, o0.elapsed_time(o1) / args.steps, dev)
+
     roof = {p: roofline_seconds(p, peaks) for p in WORKLOAD}
     value = world * 100.0 * sum(roof.values()) / (ms_step * 1e-3)
     parts = {}
@@ -480,6 +499,11 @@ def run_gpu(args):
             "parts": parts,
             "roofline": roofline,
             "roofline_allreduce_rmsnorm": roofline_ar,
+            "allreduce_rmsnorm_oneshot": {
+                "kernel": "ar_oneshot_kernel<4> (same workload, path forced; outside the step)",
+                "ms": oneshot_ms, "gbs_algorithmic": work("allreduce_rmsnorm")[1] / (oneshot_ms * 1e-3) / 1e9,
+                "frac": work("allreduce_rmsnorm")[1] / (oneshot_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                "vs_lamport_in_step": per_ms["allreduce_rmsnorm"] / oneshot_ms},
             "cpu_baseline": cpu,
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

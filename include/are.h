@@ -105,8 +105,10 @@ enum {
     ARE_DEBUG_SKIP_PUBLISH = 8u,  /* GEMM: work unit `debug_arg` never sets its ready bit */
     ARE_DEBUG_SKIP_STAGE = 16u,   /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
     ARE_DEBUG_SINGLE_CTA = 32u,   /* GEMM: use the one-CTA kernel even where the CTA-pair kernel applies */
-    ARE_DEBUG_WAIT_PROFILE = 64u  /* GEMM (CTA-pair kernel) and AR+RMSNorm: add each role's waiting SM cycles
+    ARE_DEBUG_WAIT_PROFILE = 64u, /* GEMM (CTA-pair kernel) and AR+RMSNorm: add each role's waiting SM cycles
                                      to the counters (see ARE_SNAP_COUNTERS) */
+    ARE_DEBUG_AR_ONESHOT = 128u,  /* AR+RMSNorm: take the one-shot path whatever the size (where a row fits) */
+    ARE_DEBUG_AR_LAMPORT = 256u   /* AR+RMSNorm: take the Lamport path whatever the size */
 };
 
 /* Device status word, see are_get_device_status(). */
@@ -176,6 +178,16 @@ ARE_API are_status are_workspace_reset(are_ws* ws);
 /* Change the debug switches (ARE_DEBUG_*) and their argument for later calls. */
 ARE_API are_status are_workspace_set_debug(are_ws* ws, uint32_t flags, int64_t arg);
 
+/* Per-rank input size (M * N * 2 bytes) at or below which are_allreduce_rmsnorm
+ * takes its one-shot kernel; 0 sends every call to the Lamport kernel.  The
+ * default, 448 KiB, is the crossover the pages measured for a 4-GPU collective
+ * (ROCm/aiter PR #4977, the commit that gates on the measured crossover).  With
+ * the ranks local to one GPU there is no link traffic for the Lamport path to
+ * save, and the one-shot kernel measured faster at every size, so a
+ * single-GPU caller may raise it.  Returns ARE_EINVAL for a NULL workspace,
+ * ARE_EBUSY if the workspace is in use by another thread. */
+ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t bytes);
+
 /* Synchronise the device, then copy the workspace's device status word.
  * Returns ARE_ETIMEOUT if a device wait expired, else ARE_OK. */
 ARE_API are_status are_get_device_status(are_ws* ws, are_dev_status* out);
@@ -220,6 +232,18 @@ ARE_API are_status are_gemm_ar(const are_bf16* const A[], const are_bf16* const 
  *                out = bf16( h * rsqrt(mean_j(h_j^2) + eps) * gamma ).
  * eps must be finite and > 0.  The staging buffer must have been armed (it is
  * at creation, and every call re-arms what it consumed).
+ *
+ * Two kernels compute it, with the same arithmetic in the same order, so the
+ * result bits do not depend on which runs (ROCm/aiter PR #4977, the commits
+ * that re-baseline against the one-stage kernel and gate on the crossover):
+ *  - the one-shot kernel: reads every rank's row once and stages nothing.  It
+ *    runs when the per-rank input M * N * 2 bytes is at most the workspace's
+ *    one-shot threshold (default 448 KiB; see
+ *    are_workspace_set_oneshot_max_bytes) and (R + 1) rows of N fit one
+ *    block's shared memory (R * N * 2 + N * 2 <= ~227 KB);
+ *  - the Lamport kernel (two phases meeting through the -0.0-armed staging
+ *    words) otherwise.
+ * ARE_DEBUG_AR_ONESHOT / ARE_DEBUG_AR_LAMPORT force one path.
  */
 ARE_API are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
                                  float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream);

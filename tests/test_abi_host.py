@@ -68,6 +68,7 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert lib.are_workspace_create(None, None) == are.EINVAL
     assert lib.are_workspace_destroy(None) == are.OK
     assert lib.are_workspace_reset(None) == are.EINVAL
+    assert lib.are_workspace_set_oneshot_max_bytes(None, 0) == are.EINVAL
 
 
 def test_workspace_create_validates_caps(lib):

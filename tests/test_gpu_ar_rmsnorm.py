@@ -1,4 +1,5 @@
-"""AR + residual + RMSNorm on the GPU (Lamport kernel) against the CPU oracle."""
+"""AR + residual + RMSNorm on the GPU against the CPU oracle: the Lamport
+kernel, and for small messages the one-shot kernel the dispatch picks there."""
 import numpy as np
 import pytest
 
@@ -39,13 +40,21 @@ def staging_words(ws, M, N):
     return ws.snapshot(are.SNAP_STAGING, M * N * 4).view(np.uint32).reshape(M, N)
 
 
+@pytest.mark.parametrize("path", ["default", "lamport", "oneshot"])
 @pytest.mark.parametrize("M", [1, 16, 128, 1024, 4096])
-def test_workload_shapes(ws, oracle, M):
-    """R=8 bf16 partials [M, 7168], 1% -0.0 entries, residual, gamma ~ N(1, 0.1)."""
+def test_workload_shapes(ws, oracle, M, path):
+    """R=8 bf16 partials [M, 7168], 1% -0.0 entries, residual, gamma ~ N(1, 0.1),
+    through the default dispatch and through each path forced."""
+    import all_reduce_epilogue_gb300 as are
+    flags = {"default": 0, "lamport": are.DEBUG_AR_LAMPORT, "oneshot": are.DEBUG_AR_ONESHOT}[path]
     parts, res, gamma = synth.ar_inputs(8, M, 7168, synth.config_seed(3))
-    got = run(ws, parts, res, gamma)
+    ws.set_debug(flags)
+    try:
+        got = run(ws, parts, res, gamma)
+    finally:
+        ws.set_debug(0)
     ref = oracle.allreduce_rmsnorm(parts, res, gamma, 1e-6)
-    oracle_mod_check(got, ref, f"M={M}")
+    oracle_mod_check(got, ref, f"M={M} {path}")
     # every staged word consumed and re-armed with -0.0 (the ring's odd-lap
     # sentinel never survives a call)
     assert np.all(staging_words(ws, M, 7168) == SENT)
@@ -87,7 +96,7 @@ def test_staging_snapshot_bit_exact(oracle):
     res = synth.normal_bf16((M, N), 4, synth.T_RESIDUAL)
     gamma = synth.normal_f32((N,), 4, synth.T_GAMMA, 0, 1.0, 0.1)
     with are.Workspace(R_max=8, M_max=64, N_max=N, timeout_ns=50_000_000,
-                       debug_flags=are.DEBUG_NO_REARM | are.DEBUG_COUNT_CANON) as w:
+                       debug_flags=are.DEBUG_NO_REARM | are.DEBUG_COUNT_CANON | are.DEBUG_AR_LAMPORT) as w:
         got = run(w, parts, res, gamma)
         s_ref, count = oracle.ar_stage(parts)
         snap = staging_words(w, M, N)
@@ -136,7 +145,7 @@ def test_missing_pack_times_out_and_reset_recovers(oracle):
     parts, res, gamma = synth.ar_inputs(4, M, N, 9)
     with are.Workspace(R_max=8, M_max=64, N_max=N, timeout_ns=20_000_000) as w:
         pack = 5 * (N // 8) + 17  # row 5, pack 17
-        w.set_debug(are.DEBUG_SKIP_STAGE, pack)
+        w.set_debug(are.DEBUG_SKIP_STAGE | are.DEBUG_AR_LAMPORT, pack)
         import torch
         out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         are.allreduce_rmsnorm([dev_bf16(x) for x in parts], dev_bf16(res), torch.from_numpy(gamma).cuda(), 1e-6,
