@@ -55,6 +55,8 @@ def _load(plant: int = 0):
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.oracle_bf16_rne.restype = ctypes.c_uint16
         lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        lib.oracle_bf16_rne_n.restype = None
+        lib.oracle_bf16_rne_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_max_threads.restype = i32
         lib.oracle_partial_gemm.argtypes = [vp, vp, i64, i64, i64, vp, i32]
         lib.oracle_gemm_reduce_rows.argtypes = [vp, vp, i32, i64, i64, i64, vp, i64, i32, vp, i32]
@@ -101,6 +103,13 @@ class Oracle:
         for i, v in enumerate(flat):
             out[i] = self.lib.oracle_bf16_rne(ctypes.c_float(float(v)))
         return out.reshape(x.shape)
+
+    def bf16_rne_array(self, x) -> np.ndarray:
+        """fp32 -> bf16 bits for a whole array (the same rounding function)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        out = np.empty(x.shape, dtype=np.uint16)
+        self.lib.oracle_bf16_rne_n(x.ctypes.data, out.ctypes.data, x.size)
+        return out
 
     # -- GEMM ---------------------------------------------------------------
     def partial_gemm(self, A, B) -> np.ndarray:
@@ -186,6 +195,15 @@ class Oracle:
     def allreduce_rmsnorm(self, x_list, residual, gamma, eps: float):
         s, _ = self.ar_stage(x_list)
         return self.rmsnorm(s, residual, gamma, eps)
+
+    def allreduce_residual_out(self, x_list, residual):
+        """The updated residual stream a fused add-RMSNorm hands to the next
+        layer: bf16 bits of h = canon(sum_r x_r) + residual (fp32 add; residual
+        may be None), h as the RMSNorm step defines it."""
+        s, _ = self.ar_stage(x_list)
+        M, N = s.shape
+        _, h = self.rmsnorm(s, residual, np.ones(N, np.float32), 1e-6, return_h=True)
+        return self.bf16_rne_array(h)
 
 
 _default = None

@@ -69,6 +69,11 @@ uint16_t oracle_bf16_rne(float f) {
     return (uint16_t)upper;
 }
 
+/* oracle_bf16_rne applied to n floats (the same function, element by element). */
+void oracle_bf16_rne_n(const float *x, uint16_t *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne(x[i]);
+}
+
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);

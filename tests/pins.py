@@ -313,10 +313,42 @@ def pin_rmsnorm_closed_forms(o):
     assert np.allclose(y, y2, rtol=1e-6, atol=1e-7), "scale invariance"
 
 
+def pin_bf16_rne_array(o):
+    """The array rounding is the scalar function element by element, and both
+    agree with torch's bf16 conversion (finite values, ties included)."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(4096) * 100).astype(np.float32)
+    ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 2.0 ** 100 * (1 + 2.0 ** -8)], np.float32)
+    x = np.concatenate([x, ties, np.array([0.0, -0.0, np.inf, -np.inf], np.float32)])
+    got = o.bf16_rne_array(x)
+    assert np.array_equal(got, o.bf16_rne(x)), "array rounding differs from the scalar function"
+    assert np.array_equal(got, to_bf16_bits(x)), "array rounding differs from torch"
+
+
+def pin_residual_out(o):
+    """bf16(h), h = canon(sum_r x_r) + residual:
+    R = 1 and no residual is the identity except -0.0 -> +0.0;
+    a residual equal to -x_0 gives +0.0 everywhere;
+    small-integer inputs give the exact integer sum."""
+    rng = np.random.default_rng(22)
+    x0 = synth.normal_bf16((5, 64), 23, synth.T_PARTIAL, 0)
+    x0.reshape(-1)[rng.choice(320, 20, replace=False)] = 0x8000
+    want = x0.copy()
+    want[want == 0x8000] = 0
+    assert np.array_equal(o.allreduce_residual_out([x0], None), want), "R=1 identity"
+    neg = x0 ^ np.uint16(0x8000)
+    assert np.all(o.allreduce_residual_out([x0], neg) == 0), "x - x must be +0.0"
+    ints = [rng.integers(-8, 9, size=(3, 40)) for _ in range(4)]
+    res = rng.integers(-8, 9, size=(3, 40))
+    got = f32(o.allreduce_residual_out([to_bf16_bits(a.astype(np.float32)) for a in ints],
+                                       to_bf16_bits(res.astype(np.float32))))
+    assert np.array_equal(got, (sum(ints) + res).astype(np.float32)), "integer sums"
+
+
 ALL_PINS = [
     pin_bf16_rne, pin_partial_vs_fp64, pin_partial_exact_integers, pin_partial_rectangular,
     pin_rs_vs_fp64, pin_rs_identity_ring_order, pin_rs_one_hot, pin_rs_rows_subset, pin_ar_rounds_partials,
     pin_owner_pieces_golden, pin_owner_pieces_partition, pin_masks_golden,
     pin_sentinels_golden, pin_stage_r1_and_order,
-    pin_rmsnorm_vs_torch, pin_rmsnorm_closed_forms,
+    pin_rmsnorm_vs_torch, pin_rmsnorm_closed_forms, pin_bf16_rne_array, pin_residual_out,
 ]
