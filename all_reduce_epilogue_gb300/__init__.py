@@ -42,7 +42,8 @@ EXPORTS = [
     "are_version", "are_status_string", "are_supports", "are_workspace_create", "are_workspace_destroy",
     "are_workspace_reset", "are_workspace_set_debug", "are_workspace_set_oneshot_max_bytes",
     "are_get_device_status", "are_debug_snapshot",
-    "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_rmsnorm_noalloc",
+    "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_add_rmsnorm",
+    "are_allreduce_rmsnorm_noalloc",
 ]
 
 
@@ -105,6 +106,8 @@ def load_library(path: str = LIB_PATH):
         f.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp]
     lib.are_allreduce_rmsnorm.restype = i32
     lib.are_allreduce_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i64, i64, vp, vp]
+    lib.are_allreduce_add_rmsnorm.restype = i32
+    lib.are_allreduce_add_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, i64, i64, vp, vp]
     lib.are_allreduce_rmsnorm_noalloc.restype = i32
     lib.are_allreduce_rmsnorm_noalloc.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i64, i64, vp]
     _lib = lib
@@ -267,6 +270,29 @@ def allreduce_rmsnorm(partials: Sequence, residual, gamma, eps: float, out, ws: 
         _ptrs(partials), residual.data_ptr() if residual is not None else None, gamma.data_ptr(), float(eps),
         out.data_ptr(), R, M, N, ws.handle, _stream_handle(stream))
     _check(rc, "are_allreduce_rmsnorm")
+
+
+def allreduce_add_rmsnorm(partials: Sequence, residual, gamma, eps: float, out, residual_out, ws: Workspace,
+                          stream=None):
+    """As ``allreduce_rmsnorm``, and residual_out = bf16(sum_r partials[r] +
+    residual), the residual the next layer takes (may be ``residual`` itself)."""
+    import torch
+    R = len(partials)
+    M, N = partials[0].shape
+    for t in partials:
+        _check_bf16(t, "partials")
+    if residual is not None:
+        _check_bf16(residual, "residual")
+    _check_bf16(out, "out")
+    if residual_out is not None:
+        _check_bf16(residual_out, "residual_out")
+    if gamma.dtype != torch.float32 or not gamma.is_cuda or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous CUDA float32 tensor")
+    rc = load_library().are_allreduce_add_rmsnorm(
+        _ptrs(partials), residual.data_ptr() if residual is not None else None, gamma.data_ptr(), float(eps),
+        out.data_ptr(), residual_out.data_ptr() if residual_out is not None else None, R, M, N, ws.handle,
+        _stream_handle(stream))
+    _check(rc, "are_allreduce_add_rmsnorm")
 
 
 def allreduce_rmsnorm_noalloc(partials: Sequence, residual, gamma, eps: float, out, stream=None):

@@ -399,9 +399,15 @@ are_status are_gemm_ar(const are_bf16* const A[], const are_bf16* const B[], are
     return gemm_call(kModeAR, A, B, out, R, M, N, K, ws, stream);
 }
 
-are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
-                                 float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream) {
+}  // extern "C"
+
+namespace {
+
+are_status allreduce_rmsnorm_call(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
+                                  float eps, are_bf16* out, are_bf16* residual_out, int R, int64_t M, int64_t N,
+                                  are_ws* ws, void* stream) {
     if (!ws || !partials) return ARE_EINVAL;
+    if (residual_out && !ptr_ok(residual_out, M * N)) return ARE_EINVAL;
     are_status st = are_supports(ARE_OP_ALLREDUCE_RMSNORM, R, M, N, 0);
     if (st != ARE_OK) return st;
     for (int r = 0; r < R; ++r)
@@ -421,6 +427,7 @@ are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf1
     p.residual = residual;
     p.gamma = gamma;
     p.out = out;
+    p.residual_out = residual_out;
     p.staging = ws->d_staging;
     p.status = ws->d_status;
     p.counters = ws->d_counters;
@@ -454,6 +461,21 @@ are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf1
         return from_cuda(launch_ar_oneshot(p, ppt, os_grid, s));
     }
     return from_cuda(launch_ar_rmsnorm(p, ppt, grid, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
+                                 float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream) {
+    return allreduce_rmsnorm_call(partials, residual, gamma, eps, out, nullptr, R, M, N, ws, stream);
+}
+
+are_status are_allreduce_add_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
+                                     float eps, are_bf16* out, are_bf16* residual_out, int R, int64_t M, int64_t N,
+                                     are_ws* ws, void* stream) {
+    return allreduce_rmsnorm_call(partials, residual, gamma, eps, out, residual_out, R, M, N, ws, stream);
 }
 
 }  // extern "C"

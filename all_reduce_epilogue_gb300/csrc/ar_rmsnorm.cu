@@ -278,6 +278,11 @@ __device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, in
             }
 #pragma unroll
             for (int i = 0; i < 8; ++i) ss = fmaf(f[i], f[i], ss);
+            if (p.residual_out) {  // the updated residual stream, bf16(h)
+                const uint4 hv = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                            pack_bf16x2(f[6], f[7]));
+                ptx::st_stream_v4(p.residual_out + row * (int64_t)p.N + pk * 8, hv);
+            }
             lo[k] = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                                __float_as_uint(f[3]));
             hi[k] = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
@@ -624,6 +629,11 @@ __global__ void __launch_bounds__(kOsThreads, 1) ar_oneshot_kernel(const __grid_
                 }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) ss = fmaf(h[k][i], h[k][i], ss);
+                if (p.residual_out) {  // the updated residual stream, bf16(h)
+                    const uint4 hv = make_uint4(pack_bf16x2(h[k][0], h[k][1]), pack_bf16x2(h[k][2], h[k][3]),
+                                                pack_bf16x2(h[k][4], h[k][5]), pack_bf16x2(h[k][6], h[k][7]));
+                    ptx::st_stream_v4(p.residual_out + row * (int64_t)p.N + pk * 8, hv);
+                }
             }
         }
         __syncthreads();  // every read of this row's shared copies is done

@@ -38,6 +38,7 @@ struct ArParams {
     const uint16_t* residual;      // bf16 [M, N] or nullptr
     const float* gamma;            // fp32 [N]
     uint16_t* out;                 // bf16 [M, N]
+    uint16_t* residual_out;        // bf16 [M, N] or nullptr: bf16(h), h = canon(s) + residual
     uint32_t* staging;             // fp32 words, armed with the sentinel (chunk rows, see ring_slots)
     DevStatus* status;
     unsigned long long* counters;  // debug counters

@@ -249,6 +249,25 @@ ARE_API are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const
                                  float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream);
 
 /*
+ * All-reduce + residual add + RMSNorm that also returns the updated residual.
+ * (The pages name the fused kernel's other variants but port only this
+ * operation's normalised output: ROCm/aiter PR #4977, "Known gaps /
+ * follow-ups".)  A transformer layer feeds h, the sum of the all-reduced
+ * partials and the incoming residual, to the next layer as its residual.
+ *  Arguments   : as are_allreduce_rmsnorm, plus
+ *  residual_out: bf16 [M, N] or NULL; receives bf16(h) (round to nearest even)
+ *                with h exactly as in the RMSNorm: h = s + f32(residual), s
+ *                the canonicalised fp32 ring-order sum.  It may be the same
+ *                buffer as `residual` (in-place update): each row's residual
+ *                is read before that row's residual_out is written, by the
+ *                same block.  It must not alias a partial or `out`.
+ * Both kernels (one-shot and Lamport) write it, with identical bits.
+ */
+ARE_API are_status are_allreduce_add_rmsnorm(const are_bf16* const partials[], const are_bf16* residual,
+                                             const float* gamma, float eps, are_bf16* out, are_bf16* residual_out,
+                                             int R, int64_t M, int64_t N, are_ws* ws, void* stream);
+
+/*
  * All-reduce + residual + RMSNorm that allocates nothing.
  *
  * The pages have no counterpart to this entry point.  It is for callers that

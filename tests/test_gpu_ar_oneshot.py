@@ -131,3 +131,34 @@ def test_oneshot_many_rows_per_block(oracle):
         out = call(ws, [dev_bf16(x) for x in parts], dev_bf16(res), torch.from_numpy(gamma).cuda(), M, N,
                    are.DEBUG_AR_ONESHOT)
     check_close(host_f32(out), oracle.allreduce_rmsnorm(parts, res, gamma, 1e-6), "one-shot M=1000")
+
+
+@pytest.mark.parametrize("path", ["oneshot", "lamport"])
+@pytest.mark.parametrize("R,M,N,resid,inplace", [(8, 16, 7168, True, False), (8, 300, 7168, True, True),
+                                                  (3, 5, 1024, False, False), (8, 1500, 7168, True, True)])
+def test_residual_out_bit_exact(oracle, path, R, M, N, resid, inplace):
+    """residual_out = bf16(canon(sum) + residual) bit for bit against the
+    oracle, through each kernel, also written in place over the residual; the
+    normalised output is unchanged by asking for it."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    parts, res, gamma = synth.ar_inputs(R, M, N, 6000 + R * M + N)
+    want_h = oracle.allreduce_residual_out(parts, res if resid else None)
+    with are.Workspace(R_max=8, M_max=M, N_max=N, timeout_ns=100_000_000) as ws:
+        ws.set_debug(are.DEBUG_AR_ONESHOT if path == "oneshot" else are.DEBUG_AR_LAMPORT)
+        P = [dev_bf16(x) for x in parts]
+        g = torch.from_numpy(gamma).cuda()
+        r = dev_bf16(res) if resid else None
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ro = r if (inplace and resid) else torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        are.allreduce_add_rmsnorm(P, r, g, 1e-6, out, ro, ws)
+        out2 = torch.empty_like(out)
+        r2 = dev_bf16(res) if resid else None
+        are.allreduce_rmsnorm(P, r2, g, 1e-6, out2, ws)
+        st = ws.device_status()
+    assert st["code"] == 0, st
+    assert np.array_equal(host_bits(ro), want_h), "residual_out differs from the oracle"
+    assert np.array_equal(host_bits(out), host_bits(out2)), "asking for residual_out changed out"
+    check_close(host_f32(out), oracle.allreduce_rmsnorm(parts, res if resid else None, gamma, 1e-6), "add-rmsnorm")
