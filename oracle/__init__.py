@@ -55,6 +55,11 @@ def _load(plant: int = 0):
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.oracle_bf16_rne.restype = ctypes.c_uint16
         lib.oracle_bf16_rne.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_rne_sat.restype = ctypes.c_uint8
+        lib.oracle_e4m3_rne_sat.argtypes = [ctypes.c_float]
+        lib.oracle_quant_rows.restype = None
+        lib.oracle_quant_rows.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         lib.oracle_bf16_rne_n.restype = None
         lib.oracle_bf16_rne_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
         lib.oracle_max_threads.restype = i32
@@ -195,6 +200,31 @@ class Oracle:
     def allreduce_rmsnorm(self, x_list, residual, gamma, eps: float):
         s, _ = self.ar_stage(x_list)
         return self.rmsnorm(s, residual, gamma, eps)
+
+    def e4m3(self, x) -> np.ndarray:
+        """fp32 -> FP8 E4M3 codes (RNE, saturating), element by element."""
+        x = np.asarray(x, dtype=np.float32)
+        flat = x.reshape(-1)
+        out = np.empty(flat.shape, dtype=np.uint8)
+        for i, v in enumerate(flat):
+            out[i] = self.lib.oracle_e4m3_rne_sat(ctypes.c_float(float(v)))
+        return out.reshape(x.shape)
+
+    def quant_rows(self, y):
+        """(q, scale, x): per-row dynamic FP8 E4M3 quantisation of y [M, N]:
+        scale = amax/448, x = y/scale, q = e4m3(x)."""
+        y = np.ascontiguousarray(y, dtype=np.float32)
+        M, N = y.shape
+        q = np.empty((M, N), dtype=np.uint8)
+        scale = np.empty(M, dtype=np.float32)
+        x = np.empty((M, N), dtype=np.float32)
+        self.lib.oracle_quant_rows(y.ctypes.data, M, N, q.ctypes.data, scale.ctypes.data, x.ctypes.data,
+                                   self.nthreads)
+        return q, scale, x
+
+    def allreduce_rmsnorm_quant(self, x_list, residual, gamma, eps: float):
+        """The quantising variant: (q, scale, x) of the RMSNorm output."""
+        return self.quant_rows(self.allreduce_rmsnorm(x_list, residual, gamma, eps))
 
     def allreduce_residual_out(self, x_list, residual):
         """The updated residual stream a fused add-RMSNorm hands to the next

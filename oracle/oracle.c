@@ -74,6 +74,68 @@ void oracle_bf16_rne_n(const float *x, uint16_t *out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_rne(x[i]);
 }
 
+static void set_threads(int nthreads);
+
+/*
+ * fp32 -> FP8 E4M3 (OCP "e4m3fn": bias 7, no infinities, max finite 448 =
+ * code 0x7E, NaN = 0x7F), round to nearest even, saturating to +-448.  Written
+ * from the format's definition on the fp32 bits.
+ */
+uint8_t oracle_e4m3_rne_sat(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    const uint8_t sign = (uint8_t)((x >> 24) & 0x80u);
+    const uint32_t E = (x >> 23) & 0xFFu, Mt = x & 0x7FFFFFu;
+    if (E == 0xFFu && Mt != 0) return (uint8_t)(sign | 0x7Fu);  /* NaN */
+    if (E == 0xFFu) return (uint8_t)(sign | 0x7Eu);              /* +-inf saturates */
+    if (E == 0) return sign;                                     /* fp32 zero or subnormal: below 2^-10 */
+    const int e = (int)E - 127;
+    const uint64_t sig = (1ull << 23) | Mt;                      /* value = sig * 2^(e-23) */
+    uint32_t code;
+    if (e >= -6) {                                               /* e4m3 normal range */
+        uint64_t q = sig >> 20, rem = sig & ((1ull << 20) - 1), half = 1ull << 19;
+        if (rem > half || (rem == half && (q & 1u))) ++q;        /* q in [8, 16] */
+        int ee = e;
+        if (q == 16) { q = 8; ++ee; }
+        const int be = ee + 7;
+        if (be > 15 || (be == 15 && (q & 7u) > 6)) return (uint8_t)(sign | 0x7Eu);
+        code = ((uint32_t)be << 3) | (uint32_t)(q & 7u);
+    } else {                                                     /* subnormal: units of 2^-9 */
+        const int shift = 14 - e;                                /* value / 2^-9 = sig / 2^shift */
+        if (shift >= 63) return sign;
+        uint64_t q = sig >> shift, rem = sig & ((1ull << shift) - 1), half = 1ull << (shift - 1);
+        if (rem > half || (rem == half && (q & 1u))) ++q;        /* q in [0, 8]; 8 is 2^-6, code 0x08 */
+        code = (uint32_t)q;
+    }
+    return (uint8_t)(sign | code);
+}
+
+/*
+ * The quantising variant of the RMSNorm step, per row (dynamic, per token):
+ *   y_j   = h_j / sqrt(ms + eps) * gamma_j     (as oracle_rmsnorm_rows, fp32)
+ *   amax  = max_j |y_j|;  scale = amax / 448 (fp32 division; 1 if amax == 0)
+ *   q_j   = e4m3(y_j / scale)                  (fp32 division, RNE, saturating)
+ * x (optional) receives y_j / scale, the value each code rounds.
+ */
+void oracle_quant_rows(const float *y, int64_t M, int64_t N, uint8_t *q, float *scale, float *x, int nthreads) {
+    set_threads(nthreads);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < M; ++i) {
+        float amax = 0.0f;
+        for (int64_t j = 0; j < N; ++j) {
+            const float a = fabsf(y[i * N + j]);
+            if (a > amax) amax = a;
+        }
+        const float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+        scale[i] = sc;
+        for (int64_t j = 0; j < N; ++j) {
+            const float v = y[i * N + j] / sc;
+            if (x) x[i * N + j] = v;
+            q[i * N + j] = oracle_e4m3_rne_sat(v);
+        }
+    }
+}
+
 static void set_threads(int nthreads) {
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);

@@ -345,10 +345,52 @@ def pin_residual_out(o):
     assert np.array_equal(got, (sum(ints) + res).astype(np.float32)), "integer sums"
 
 
+def pin_e4m3_vs_torch(o):
+    """FP8 E4M3 rounding agrees with torch's float8_e4m3fn conversion on
+    finite values within range (normals, subnormals, exact ties), and
+    saturates what torch turns into NaN."""
+    rng = np.random.default_rng(31)
+    mags = 2.0 ** rng.uniform(-12, 8.8, 6000)
+    x = (mags * rng.choice([-1.0, 1.0], 6000)).astype(np.float32)
+    ties = []
+    for e in range(-6, 9):  # halfway between neighbouring codes, both parities of the lower one
+        for m in range(8):
+            lo = (1 + m / 8) * 2.0 ** e
+            ties.append(lo + 2.0 ** e / 16)
+    ties += [(k + 0.5) * 2.0 ** -9 for k in range(8)]  # subnormal ties
+    x = np.concatenate([x, np.array(ties, np.float32), -np.array(ties, np.float32)])
+    x = x[np.abs(x) <= 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(o.e4m3(x), want), "e4m3 rounding differs from torch"
+    sat = o.e4m3(np.array([464.0, 1e6, np.inf, -1e30, -np.inf], np.float32))
+    assert list(sat) == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE], "saturation"
+    assert o.e4m3(np.array([np.nan], np.float32))[0] & 0x7F == 0x7F, "NaN"
+
+
+def pin_quant_rows(o):
+    """Per-row dynamic quantisation: the largest |y| maps to +-448 (code 0x7E);
+    dequantised codes are within half an E4M3 step (2^-4 relative) of y where
+    y/scale is a normal E4M3 value; a zero row gets scale 1 and zero codes."""
+    rng = np.random.default_rng(32)
+    y = (rng.standard_normal((5, 700)) * rng.uniform(0.01, 50, (5, 1))).astype(np.float32)
+    y[4] = 0
+    q, scale, x = o.quant_rows(y)
+    assert scale[4] == 1 and np.all(q[4] == 0), "zero row"
+    for i in range(4):
+        j = int(np.argmax(np.abs(y[i])))
+        assert q[i, j] & 0x7F == 0x7E, "amax element is not +-448"
+        vals = torch.from_numpy(q[i].copy()).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+        deq = vals.astype(np.float64) * float(scale[i])
+        normal = np.abs(x[i]) >= 2.0 ** -6
+        err = np.abs(deq - y[i]) / np.abs(y[i].astype(np.float64))
+        assert np.all(err[normal] <= 2.0 ** -4 * (1 + 1e-6)), "dequantised value off by more than half a step"
+
+
 ALL_PINS = [
     pin_bf16_rne, pin_partial_vs_fp64, pin_partial_exact_integers, pin_partial_rectangular,
     pin_rs_vs_fp64, pin_rs_identity_ring_order, pin_rs_one_hot, pin_rs_rows_subset, pin_ar_rounds_partials,
     pin_owner_pieces_golden, pin_owner_pieces_partition, pin_masks_golden,
     pin_sentinels_golden, pin_stage_r1_and_order,
     pin_rmsnorm_vs_torch, pin_rmsnorm_closed_forms, pin_bf16_rne_array, pin_residual_out,
+    pin_e4m3_vs_torch, pin_quant_rows,
 ]
