@@ -42,7 +42,7 @@ EXPORTS = [
     "are_version", "are_status_string", "are_supports", "are_workspace_create", "are_workspace_destroy",
     "are_workspace_reset", "are_workspace_set_debug", "are_workspace_set_oneshot_max_bytes",
     "are_get_device_status", "are_debug_snapshot",
-    "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_add_rmsnorm",
+    "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_add_rmsnorm", "are_allreduce_rmsnorm_quant",
     "are_allreduce_rmsnorm_noalloc",
 ]
 
@@ -108,6 +108,8 @@ def load_library(path: str = LIB_PATH):
     lib.are_allreduce_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i64, i64, vp, vp]
     lib.are_allreduce_add_rmsnorm.restype = i32
     lib.are_allreduce_add_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, i32, i64, i64, vp, vp]
+    lib.are_allreduce_rmsnorm_quant.restype = i32
+    lib.are_allreduce_rmsnorm_quant.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i64, i64, vp, vp]
     lib.are_allreduce_rmsnorm_noalloc.restype = i32
     lib.are_allreduce_rmsnorm_noalloc.argtypes = [vp, vp, vp, ctypes.c_float, vp, i32, i64, i64, vp]
     _lib = lib
@@ -293,6 +295,32 @@ def allreduce_add_rmsnorm(partials: Sequence, residual, gamma, eps: float, out, 
         out.data_ptr(), residual_out.data_ptr() if residual_out is not None else None, R, M, N, ws.handle,
         _stream_handle(stream))
     _check(rc, "are_allreduce_add_rmsnorm")
+
+
+def allreduce_rmsnorm_quant(partials: Sequence, residual, gamma, eps: float, out_q, out_scale, ws: Workspace,
+                            residual_out=None, stream=None):
+    """Quantising variant: out_q (uint8 FP8 E4M3 codes [M, N]) and out_scale
+    (fp32 [M]) with y ~= e4m3(out_q) * out_scale per row; residual_out optional."""
+    import torch
+    R = len(partials)
+    M, N = partials[0].shape
+    for t in partials:
+        _check_bf16(t, "partials")
+    if residual is not None:
+        _check_bf16(residual, "residual")
+    if residual_out is not None:
+        _check_bf16(residual_out, "residual_out")
+    if out_q.dtype != torch.uint8 or not out_q.is_cuda or not out_q.is_contiguous():
+        raise ValueError("out_q must be a contiguous CUDA uint8 tensor")
+    if out_scale.dtype != torch.float32 or not out_scale.is_cuda or not out_scale.is_contiguous():
+        raise ValueError("out_scale must be a contiguous CUDA float32 tensor")
+    if gamma.dtype != torch.float32 or not gamma.is_cuda or not gamma.is_contiguous():
+        raise ValueError("gamma must be a contiguous CUDA float32 tensor")
+    rc = load_library().are_allreduce_rmsnorm_quant(
+        _ptrs(partials), residual.data_ptr() if residual is not None else None, gamma.data_ptr(), float(eps),
+        out_q.data_ptr(), out_scale.data_ptr(), residual_out.data_ptr() if residual_out is not None else None,
+        R, M, N, ws.handle, _stream_handle(stream))
+    _check(rc, "are_allreduce_rmsnorm_quant")
 
 
 def allreduce_rmsnorm_noalloc(partials: Sequence, residual, gamma, eps: float, out, stream=None):

@@ -404,15 +404,17 @@ are_status are_gemm_ar(const are_bf16* const A[], const are_bf16* const B[], are
 namespace {
 
 are_status allreduce_rmsnorm_call(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
-                                  float eps, are_bf16* out, are_bf16* residual_out, int R, int64_t M, int64_t N,
-                                  are_ws* ws, void* stream) {
+                                  float eps, are_bf16* out, are_bf16* residual_out, uint8_t* out_q, float* out_scale,
+                                  int R, int64_t M, int64_t N, are_ws* ws, void* stream) {
     if (!ws || !partials) return ARE_EINVAL;
     if (residual_out && !ptr_ok(residual_out, M * N)) return ARE_EINVAL;
+    const bool quant = out_q != nullptr || out_scale != nullptr;
+    if (quant && (!ptr_ok(out_q, M * N) || !ptr_ok(out_scale, M))) return ARE_EINVAL;
     are_status st = are_supports(ARE_OP_ALLREDUCE_RMSNORM, R, M, N, 0);
     if (st != ARE_OK) return st;
     for (int r = 0; r < R; ++r)
         if (!ptr_ok(partials[r], M * N)) return ARE_EINVAL;
-    if ((residual && !aligned16(residual)) || !ptr_ok(gamma, N) || !ptr_ok(out, M * N)) return ARE_EINVAL;
+    if ((residual && !aligned16(residual)) || !ptr_ok(gamma, N) || (!quant && !ptr_ok(out, M * N))) return ARE_EINVAL;
     if (!(eps > 0.f) || !std::isfinite(eps)) return ARE_EINVAL;
     TryLock lk(ws->mu);
     if (!lk.ok) return ARE_EBUSY;
@@ -428,6 +430,8 @@ are_status allreduce_rmsnorm_call(const are_bf16* const partials[], const are_bf
     p.gamma = gamma;
     p.out = out;
     p.residual_out = residual_out;
+    p.out_q = out_q;
+    p.out_scale = out_scale;
     p.staging = ws->d_staging;
     p.status = ws->d_status;
     p.counters = ws->d_counters;
@@ -469,13 +473,21 @@ extern "C" {
 
 are_status are_allreduce_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
                                  float eps, are_bf16* out, int R, int64_t M, int64_t N, are_ws* ws, void* stream) {
-    return allreduce_rmsnorm_call(partials, residual, gamma, eps, out, nullptr, R, M, N, ws, stream);
+    return allreduce_rmsnorm_call(partials, residual, gamma, eps, out, nullptr, nullptr, nullptr, R, M, N, ws, stream);
 }
 
 are_status are_allreduce_add_rmsnorm(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
                                      float eps, are_bf16* out, are_bf16* residual_out, int R, int64_t M, int64_t N,
                                      are_ws* ws, void* stream) {
-    return allreduce_rmsnorm_call(partials, residual, gamma, eps, out, residual_out, R, M, N, ws, stream);
+    return allreduce_rmsnorm_call(partials, residual, gamma, eps, out, residual_out, nullptr, nullptr, R, M, N, ws,
+                                  stream);
+}
+
+are_status are_allreduce_rmsnorm_quant(const are_bf16* const partials[], const are_bf16* residual, const float* gamma,
+                                       float eps, uint8_t* out_q, float* out_scale, are_bf16* residual_out, int R,
+                                       int64_t M, int64_t N, are_ws* ws, void* stream) {
+    return allreduce_rmsnorm_call(partials, residual, gamma, eps, nullptr, residual_out, out_q, out_scale, R, M, N,
+                                  ws, stream);
 }
 
 }  // extern "C"

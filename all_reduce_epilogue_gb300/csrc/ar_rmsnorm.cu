@@ -37,6 +37,7 @@
 // come from the copy engine, not from registers.  The staging words
 // are fp32: staging a bf16 sum would round before the residual add.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include "are_internal.h"
 #include "ptx.cuh"
@@ -97,7 +98,7 @@ struct Shared {
     uint64_t* empty;    // [stages]
     uint64_t* rfull;    // [kResSlots]
     uint64_t* rempty;   // [kResSlots]
-    float* red;         // [16]
+    float* red;         // [32]: block sums in 0..8, block maxima in 16..24
     volatile int* bdone;        // chunks phase B has finished
     volatile uint32_t* abort;   // block gave up
 };
@@ -113,7 +114,7 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const ArParams& p) {
     s.rfull = s.empty + kMaxArStages;
     s.rempty = s.rfull + kResSlots;
     s.red = reinterpret_cast<float*>(s.rempty + kResSlots);
-    s.bdone = reinterpret_cast<volatile int*>(s.red + 16);
+    s.bdone = reinterpret_cast<volatile int*>(s.red + 32);
     s.abort = reinterpret_cast<volatile uint32_t*>(s.bdone + 1);
     return s;
 }
@@ -196,6 +197,84 @@ __device__ __forceinline__ uint32_t rearm_value(const ArParams& p, int c, int i)
 __device__ __forceinline__ int consumed_row(int G) {
     int i = (int)blockIdx.x - G / 2;
     return i < 0 ? i + G : i;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// The normalised row y = h * inv * gamma leaves either as bf16 (`out`) or, in
+// the quantising variant, as FP8 E4M3 codes with one fp32 scale per row
+// (dynamic per-token quantisation: scale = max|y| / 448, code = e4m3(y / scale),
+// round to nearest even, saturating; both divisions correctly rounded).
+// NT threads hold the row's packs bt, bt + NT, ...; bar() is their barrier and
+// red[16..] their scratch.
+template <int PPT, int NT, typename Bar>
+__device__ __forceinline__ void store_row(const ArParams& p, int64_t row, int bt, const float (&h)[PPT][8], float inv,
+                                          float* red, Bar bar) {
+    const int P = p.packs_per_row;
+    if (!p.out_q) {
+#pragma unroll
+        for (int k = 0; k < PPT; ++k) {
+            const int pk = bt + k * NT;
+            if (pk < P) {
+                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
+                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+                uint4 o;
+                o.x = pack_bf16x2(h[k][0] * inv * g0.x, h[k][1] * inv * g0.y);
+                o.y = pack_bf16x2(h[k][2] * inv * g0.z, h[k][3] * inv * g0.w);
+                o.z = pack_bf16x2(h[k][4] * inv * g1.x, h[k][5] * inv * g1.y);
+                o.w = pack_bf16x2(h[k][6] * inv * g1.z, h[k][7] * inv * g1.w);
+                ptx::st_stream_v4(p.out + row * (int64_t)p.N + pk * 8, o);
+            }
+        }
+        return;
+    }
+    // y is recomputed in the second pass (same expression, same bits) rather than
+    // held in registers across the block reduction
+    float am = 0.f;
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+        const int pk = bt + k * NT;
+        if (pk < P) {
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(h[k][i] * inv * g[i]));
+        }
+    }
+    const int w = bt >> 5, lane = bt & 31;
+    am = warp_max(am);
+    if (lane == 0) red[16 + w] = am;
+    bar();
+    if (w == 0) {
+        float v = lane < NT / 32 ? red[16 + lane] : 0.f;
+        v = warp_max(v);
+        if (lane == 0) red[16 + NT / 32] = v;
+    }
+    bar();
+    const float amax = red[16 + NT / 32];
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (bt == 0) p.out_scale[row] = sc;
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+        const int pk = bt + k * NT;
+        if (pk < P) {
+            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
+            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            uint32_t c[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                c[i] = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(h[k][i] * inv * g[i], sc), __NV_SATFINITE, __NV_E4M3);
+            const uint2 v = make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
+                                       c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24));
+            ptx::st_stream_v2(p.out_q + row * (int64_t)p.N + pk * 8, v);
+        }
+    }
 }
 
 // ARE_DEBUG_WAIT_PROFILE: one thread of each role adds the SM cycles it spent
@@ -300,20 +379,15 @@ __device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, in
     }
     b_bar();
     const float inv = rsqrtf(sh.red[kBThreads / 32] * p.inv_n + p.eps);
+    float hv[PPT][8];
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-        const int pk = bt + k * kBThreads;
-        if (pk < P) {
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
-            uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(lo[k].x) * inv * g0.x, __uint_as_float(lo[k].y) * inv * g0.y);
-            o.y = pack_bf16x2(__uint_as_float(lo[k].z) * inv * g0.z, __uint_as_float(lo[k].w) * inv * g0.w);
-            o.z = pack_bf16x2(__uint_as_float(hi[k].x) * inv * g1.x, __uint_as_float(hi[k].y) * inv * g1.y);
-            o.w = pack_bf16x2(__uint_as_float(hi[k].z) * inv * g1.z, __uint_as_float(hi[k].w) * inv * g1.w);
-            ptx::st_stream_v4(p.out + row * (int64_t)p.N + pk * 8, o);
-        }
+        hv[k][0] = __uint_as_float(lo[k].x); hv[k][1] = __uint_as_float(lo[k].y);
+        hv[k][2] = __uint_as_float(lo[k].z); hv[k][3] = __uint_as_float(lo[k].w);
+        hv[k][4] = __uint_as_float(hi[k].x); hv[k][5] = __uint_as_float(hi[k].y);
+        hv[k][6] = __uint_as_float(hi[k].z); hv[k][7] = __uint_as_float(hi[k].w);
     }
+    store_row<PPT, kBThreads>(p, row, bt, hv, inv, sh.red, [] { b_bar(); });
 }
 
 template <int PPT>
@@ -648,20 +722,7 @@ __global__ void __launch_bounds__(kOsThreads, 1) ar_oneshot_kernel(const __grid_
         }
         __syncthreads();
         const float inv = rsqrtf(red[kOsThreads / 32] * p.inv_n + p.eps);
-#pragma unroll
-        for (int k = 0; k < PPT; ++k) {
-            const int pk = bt + k * kOsThreads;
-            if (pk < P) {
-                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
-                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
-                uint4 o;
-                o.x = pack_bf16x2(h[k][0] * inv * g0.x, h[k][1] * inv * g0.y);
-                o.y = pack_bf16x2(h[k][2] * inv * g0.z, h[k][3] * inv * g0.w);
-                o.z = pack_bf16x2(h[k][4] * inv * g1.x, h[k][5] * inv * g1.y);
-                o.w = pack_bf16x2(h[k][6] * inv * g1.z, h[k][7] * inv * g1.w);
-                ptx::st_stream_v4(p.out + row * (int64_t)p.N + pk * 8, o);
-            }
-        }
+        store_row<PPT, kOsThreads>(p, row, bt, h, inv, red, [] { __syncthreads(); });
         __syncthreads();  // red[] is rewritten by the next row
     }
 }
@@ -731,7 +792,7 @@ cudaError_t launch_ar_rmsnorm(const ArParams& p, int ppt, int grid, cudaStream_t
 }
 
 size_t ar_oneshot_smem_bytes(int R, int N, bool residual) {
-    return (size_t)(R + (residual ? 1 : 0)) * (size_t)N * 2 + 8 + 16 * 4 + 64;
+    return (size_t)(R + (residual ? 1 : 0)) * (size_t)N * 2 + 8 + 32 * 4 + 64;
 }
 
 bool ar_oneshot_fits(int R, int N, bool residual) { return ar_oneshot_smem_bytes(R, N, residual) <= kSmemLimit; }

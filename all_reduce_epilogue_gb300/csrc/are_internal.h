@@ -39,6 +39,8 @@ struct ArParams {
     const float* gamma;            // fp32 [N]
     uint16_t* out;                 // bf16 [M, N]
     uint16_t* residual_out;        // bf16 [M, N] or nullptr: bf16(h), h = canon(s) + residual
+    uint8_t* out_q;                // FP8 E4M3 [M, N] or nullptr (then `out` is written)
+    float* out_scale;              // fp32 [M] with out_q: the per-row scale
     uint32_t* staging;             // fp32 words, armed with the sentinel (chunk rows, see ring_slots)
     DevStatus* status;
     unsigned long long* counters;  // debug counters

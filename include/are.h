@@ -268,6 +268,27 @@ ARE_API are_status are_allreduce_add_rmsnorm(const are_bf16* const partials[], c
                                              int R, int64_t M, int64_t N, are_ws* ws, void* stream);
 
 /*
+ * All-reduce + residual add + RMSNorm with a quantised output: the pages list
+ * the fused kernel's quantising variants without defining one (ROCm/aiter PR
+ * #4977, "Known gaps / follow-ups"); this is per-row (per-token) dynamic FP8:
+ *  out_q       : FP8 E4M3 codes [M, N] (OCP e4m3fn: bias 7, max finite 448)
+ *  out_scale   : fp32 [M]
+ *  residual_out: bf16 [M, N] or NULL, as in are_allreduce_add_rmsnorm
+ *  Result      : y = h * rsqrt(mean_j(h_j^2) + eps) * gamma as in
+ *                are_allreduce_rmsnorm (fp32, before its bf16 rounding);
+ *                out_scale[i] = max_j |y_ij| / 448 (1 for an all-zero row);
+ *                out_q[i][j]  = e4m3(y_ij / out_scale[i]), round to nearest
+ *                even, saturating to +-448; both divisions correctly rounded.
+ *                y_ij ~= out_q[i][j] * out_scale[i].
+ * The other arguments, the two kernels and their dispatch are as for
+ * are_allreduce_rmsnorm; no bf16 output is written.
+ */
+ARE_API are_status are_allreduce_rmsnorm_quant(const are_bf16* const partials[], const are_bf16* residual,
+                                               const float* gamma, float eps, uint8_t* out_q, float* out_scale,
+                                               are_bf16* residual_out, int R, int64_t M, int64_t N, are_ws* ws,
+                                               void* stream);
+
+/*
  * All-reduce + residual + RMSNorm that allocates nothing.
  *
  * The pages have no counterpart to this entry point.  It is for callers that

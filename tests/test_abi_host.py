@@ -65,6 +65,7 @@ def test_calls_reject_bad_arguments_without_launching(lib):
     assert lib.are_gemm_ar(A, A, A, 2, 64, 256, 128, None, None) == are.EINVAL
     assert lib.are_allreduce_rmsnorm(A, None, 16, ctypes.c_float(1e-6), 16, 2, 4, 64, None, None) == are.EINVAL
     assert lib.are_allreduce_add_rmsnorm(A, None, 16, ctypes.c_float(1e-6), 16, None, 2, 4, 64, None, None) == are.EINVAL
+    assert lib.are_allreduce_rmsnorm_quant(A, None, 16, ctypes.c_float(1e-6), 16, 16, None, 2, 4, 64, None, None) == are.EINVAL
     # bad workspace-independent arguments fail the same way
     assert lib.are_workspace_create(None, None) == are.EINVAL
     assert lib.are_workspace_destroy(None) == are.OK
