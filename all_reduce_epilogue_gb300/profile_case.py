@@ -26,6 +26,8 @@ def main(argv=None) -> int:
     ap.add_argument("--K", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--views", type=int, default=0, help="gemm_ar: distinct output views (default R)")
+    ap.add_argument("--path", choices=["default", "oneshot", "lamport"], default="default",
+                    help="allreduce_rmsnorm: force a kernel")
     ap.add_argument("--seed", type=int, default=0)
     a = ap.parse_args(argv)
     torch.manual_seed(a.seed)
@@ -40,6 +42,7 @@ def main(argv=None) -> int:
         gamma = 1 + 0.1 * torch.randn(a.N, device=dev)
         out = torch.empty_like(res)
         with are.Workspace(R_max=a.R, M_max=a.M, N_max=a.N) as ws:
+            ws.set_debug({"default": 0, "oneshot": are.DEBUG_AR_ONESHOT, "lamport": are.DEBUG_AR_LAMPORT}[a.path])
             for _ in range(a.iters):
                 are.allreduce_rmsnorm(parts, res, gamma, 1e-6, out, ws)
             st = ws.device_status()
