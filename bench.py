@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # each part's kernel at this workload, from one ncu capture of a bench step
 # (profiles/launch_list_bench_step.md).  Set back to None whenever that kernel's
 # source changes, until it is captured again.
-NCU_TRAFFIC = {"gemm_rs": 9933.0e6, "gemm_ar": 3558.6e6, "allreduce_rmsnorm": None}
+NCU_TRAFFIC = {"gemm_rs": 9923.4e6, "gemm_ar": 3493.3e6, "allreduce_rmsnorm": 638.3e6}
 
 
 # --------------------------------------------------------------------------- work model
