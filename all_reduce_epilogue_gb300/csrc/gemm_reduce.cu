@@ -18,7 +18,13 @@
 // rows span several owner segments is cut at the segment boundaries and each
 // piece is stored into its owner's segment.
 //
-// One-GPU design.  A work unit is (rank r, output tile t), a 128x256 tile of
+// One-GPU design.  Two kernels implement it.  gemm_pair_kernel (further down)
+// runs a CTA pair per 256x256 block with cta_group::2 MMAs and is used
+// whenever there are at least two 128-row tiles; gemm_reduce_kernel (next),
+// one CTA per 128x256 tile, covers the rest.  Both share the workspace layout,
+// the mask protocol and the owner-piece stores.
+//
+// gemm_reduce_kernel.  A work unit is (rank r, output tile t), a 128x256 tile of
 // P_r = A_r B_r with K = K_r.  Units are ordered tile-major with the tile's
 // reducer (the owner of the tile's first row for GEMM+RS, rank t mod R for
 // GEMM+AR) last among its R units; a persistent grid (one CTA per SM) walks
@@ -30,9 +36,10 @@
 // sub-tiles through the partial buffer and adds all R in the order
 // r = 0..R-1 in fp32.
 //
-// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer, warp 2
-// TMEM allocator + partial loader, warp 3 idle, warps 4-7 epilogue (TMEM lane
-// = tile row).  TMEM holds two 128x256 fp32 accumulators (512 columns).
+// Warp roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer (both run
+// converged, one elected lane issuing), warp 2 TMEM allocator + partial loader,
+// warp 3 idle, warps 4-7 epilogue (TMEM lane = tile row).  TMEM holds two
+// 128x256 fp32 accumulators (512 columns).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
