@@ -40,6 +40,12 @@
  *    time: calls on different streams with the same workspace race on the
  *    device, and a call made while another host thread is inside the library
  *    with the same workspace returns ARE_EBUSY.
+ *  - The operations (are_gemm_rs, are_gemm_ar, are_allreduce_rmsnorm and its
+ *    variants) may be captured into a CUDA graph once the workspace exists:
+ *    they only launch kernels, and the state they leave for the next call
+ *    (tile masks at 0, staging words at -0.0) is restored inside those
+ *    kernels, never by a host step, so every replay finds it as the capture
+ *    did.  Workspace creation, reset and snapshots are not capturable.
  *  - Every argument is validated before anything is launched: on any error
  *    nothing is launched and nothing is written.
  *  - Device-side waits are bounded by the workspace's timeout.  A wait that
