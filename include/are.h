@@ -40,8 +40,9 @@
  *    time: calls on different streams with the same workspace race on the
  *    device, and a call made while another host thread is inside the library
  *    with the same workspace returns ARE_EBUSY.
- *  - The operations (are_gemm_rs, are_gemm_ar, are_allreduce_rmsnorm and its
- *    variants) may be captured into a CUDA graph once the workspace exists:
+ *  - are_gemm_rs, are_gemm_ar, are_allreduce_rmsnorm, are_allreduce_add_rmsnorm
+ *    and are_allreduce_rmsnorm_quant may be captured into a CUDA graph once
+ *    their workspace exists:
  *    they only launch kernels, and the state they leave for the next call
  *    (tile masks at 0, staging words at -0.0) is restored inside those
  *    kernels, never by a host step, so every replay finds it as the capture
