@@ -42,8 +42,8 @@
  *    with the same workspace returns ARE_EBUSY.
  *  - are_gemm_rs, are_gemm_ar, are_allreduce_rmsnorm, are_allreduce_add_rmsnorm
  *    and are_allreduce_rmsnorm_quant may be captured into a CUDA graph once
- *    their workspace exists:
- *    they only launch kernels, and the state they leave for the next call
+ *    their workspace exists: they only enqueue work on `stream` (kernels;
+ *    memsets for an empty contraction), and the state they leave for the next call
  *    (tile masks at 0, staging words at -0.0) is restored inside those
  *    kernels, never by a host step, so every replay finds it as the capture
  *    did.  Workspace creation, reset and snapshots are not capturable.
