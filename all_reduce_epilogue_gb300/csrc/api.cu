@@ -207,7 +207,12 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     // CTA pairs (256-row tiles) wherever there are at least two tile rows and
     // the device can co-schedule the clusters; one CTA per tile otherwise.
     const int clusters = gemm_pair_max_clusters();
-    if (tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA)) {
+    // Below one wave of pairs the reduce of the last (only) wave is the kernel's tail, and
+    // the one-CTA kernel's deeper partial buffer (and its reducer's own partial kept in
+    // TMEM) finishes it sooner: R=4, M=256 measured 33 us against 69 us.
+    const int64_t pair_units = (int64_t)p->pairs_m * tiles_n * R;
+    const bool pair_ok = tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
+    if (pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA))) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
         // GEMM+RS: run the ranks block by block (two waves of tile pairs per block) so a
         // wave streams one or two ranks' operands; GEMM+AR keeps the ranks innermost (its

@@ -115,7 +115,9 @@ enum {
     ARE_DEBUG_WAIT_PROFILE = 64u, /* GEMM (CTA-pair kernel) and AR+RMSNorm: add each role's waiting SM cycles
                                      to the counters (see ARE_SNAP_COUNTERS) */
     ARE_DEBUG_AR_ONESHOT = 128u,  /* AR+RMSNorm: take the one-shot path whatever the size (where a row fits) */
-    ARE_DEBUG_AR_LAMPORT = 256u   /* AR+RMSNorm: take the Lamport path whatever the size */
+    ARE_DEBUG_AR_LAMPORT = 256u,  /* AR+RMSNorm: take the Lamport path whatever the size */
+    ARE_DEBUG_PAIR_CTA = 512u     /* GEMM: use the CTA-pair kernel wherever it applies (two or more tile rows),
+                                     also below one wave of pairs */
 };
 
 /* Device status word, see are_get_device_status(). */

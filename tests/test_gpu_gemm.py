@@ -125,16 +125,19 @@ def test_segments_equal_contiguous(oracle):
     assert np.array_equal(a, b)
 
 
-def test_masks_and_owner_pieces_bit_exact(oracle):
+@pytest.mark.parametrize("kernel", ["default", "pair"])
+def test_masks_and_owner_pieces_bit_exact(oracle, kernel):
     """With re-arm off, every tile's ready word is (1 << R) - 1 (and words past
     the last tile are 0); each reducer's stored owner pieces equal the
     oracle's cut of the tile at owner boundaries.  After a normal call every
-    word is 0 again."""
+    word is 0 again.  Through the default kernel choice and with the CTA-pair
+    kernel forced wherever it applies."""
     need_gpu()
     import all_reduce_epilogue_gb300 as are
+    extra = are.DEBUG_PAIR_CTA if kernel == "pair" else 0
     for (R, M, N, K) in [(2, 64, 256, 128), (4, 256, 1024, 128), (3, 264, 320, 64), (8, 1024, 512, 64)]:
         A, B = synth.gemm_inputs(R, M, N, K, 5)
-        with make_ws(debug_flags=are.DEBUG_NO_REARM | are.DEBUG_LOG_PIECES) as ws:
+        with make_ws(debug_flags=are.DEBUG_NO_REARM | are.DEBUG_LOG_PIECES | extra) as ws:
             run_rs(ws, A, B)
             T = ((M + 127) // 128) * ((N + 255) // 256)
             words = ws.snapshot(are.SNAP_MASKS, (T + 8) * 4).view(np.uint32)
@@ -148,7 +151,7 @@ def test_masks_and_owner_pieces_bit_exact(oracle):
                 got = [tuple(int(v) for v in log[t, 3 + 3 * i: 6 + 3 * i]) for i in range(n)]
                 assert got == oracle.tile_pieces(int(tm) * 128, 128, M, R), (R, M, N, t)
             assert len(seen) == T
-            ws.set_debug(0)
+            ws.set_debug(extra)
             ws.reset()
             run_rs(ws, A, B)
             assert np.all(ws.snapshot(are.SNAP_MASKS, T * 4).view(np.uint32) == 0)
@@ -164,7 +167,7 @@ def test_unpublished_tile_times_out_and_reset_recovers(oracle, single_cta):
     import all_reduce_epilogue_gb300 as are
     R, M, N, K = 4, 256, 512, 128
     A, B = synth.gemm_inputs(R, M, N, K, 8)
-    base = are.DEBUG_SINGLE_CTA if single_cta else 0
+    base = are.DEBUG_SINGLE_CTA if single_cta else are.DEBUG_PAIR_CTA
     with make_ws(timeout_ns=20_000_000) as ws:
         ws.set_debug(base | are.DEBUG_SKIP_PUBLISH, 0)
         import torch
@@ -269,7 +272,7 @@ def test_pair_kernel_matches_single_cta_kernel(mode, R, M, N, K):
     dA = [dev_bf16(a) for a in A]
     dB = [dev_bf16(b) for b in B]
     outs = []
-    for flags in (0, are.DEBUG_SINGLE_CTA):
+    for flags in (are.DEBUG_PAIR_CTA, are.DEBUG_SINGLE_CTA):
         with make_ws(M_max=M, N_max=N, K_max=K, debug_flags=flags) as ws:
             out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             if mode == "rs":
@@ -295,10 +298,11 @@ def test_wait_profile_counts_and_leaves_results_unchanged():
     dA = [dev_bf16(a) for a in A]
     dB = [dev_bf16(b) for b in B]
     with make_ws(M_max=M, N_max=N, K_max=K) as ws:
+        ws.set_debug(are.DEBUG_PAIR_CTA)
         out0 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         are.gemm_rs(dA, dB, out0, ws)
         ws.reset()
-        ws.set_debug(are.DEBUG_WAIT_PROFILE)
+        ws.set_debug(are.DEBUG_WAIT_PROFILE | are.DEBUG_PAIR_CTA)
         out1 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         are.gemm_rs(dA, dB, out1, ws)
         assert ws.device_status()["code"] == 0
