@@ -751,6 +751,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    volatile uint64_t* t_mma_end = reinterpret_cast<volatile uint64_t*>(tmem_slot + 2);  // wait profile only
+    const uint64_t t_begin = (p.flags & ARE_DEBUG_WAIT_PROFILE) ? ptx::globaltimer() : 0;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -855,6 +857,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             if (issuer) ptx::umma_commit_pair(mma_done);
             __syncwarp();
             drain_bar(mma_done, 0, p);
+            if (lane == 0 && (p.flags & ARE_DEBUG_WAIT_PROFILE)) *t_mma_end = ptx::globaltimer();
             if (lane == 0) {
                 prof_add(p, 2, w_full);
                 prof_add(p, 3, w_tempty);
@@ -1147,6 +1150,16 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     ptx::tc_fence_before();
     ptx::cluster_sync();
     ptx::tc_fence_after();
+    if (threadIdx.x == 0 && q == 0 && (p.flags & ARE_DEBUG_WAIT_PROFILE)) {
+        // the pair's time after its last MMA completed (drains and reductions still
+        // running), and its whole span, in ns
+        const uint64_t t_end = ptx::globaltimer();
+        const uint64_t tail = t_end - *t_mma_end;
+        atomicMax(&p.counters[9], (unsigned long long)tail);
+        atomicAdd(&p.counters[10], (unsigned long long)tail);
+        atomicMax(&p.counters[11], (unsigned long long)(t_end - t_begin));
+        atomicAdd(&p.counters[12], (unsigned long long)(*t_mma_end - t_begin));
+    }
     if (warp == 2) {
         __syncwarp();
         ptx::tmem_dealloc_pair(tmem_base, kTmemCols2);

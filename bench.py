@@ -50,7 +50,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # each part's kernel at this workload, from one ncu capture of a bench step
 # (profiles/launch_list_bench_step.md).  Set back to None whenever that kernel's
 # source changes, until it is captured again.
-NCU_TRAFFIC = {"gemm_rs": 9923.4e6, "gemm_ar": 3493.3e6, "allreduce_rmsnorm": 638.3e6}
+NCU_TRAFFIC = {"gemm_rs": 9935.3e6, "gemm_ar": 3557.5e6, "allreduce_rmsnorm": 639.2e6}
 
 
 # --------------------------------------------------------------------------- work model
@@ -356,24 +356,30 @@ def run_gpu(args):
     ms_step = max_over_ranks(dist, total_ms / args.steps, dev)
     per_ms = {p: statistics.mean(v) for p, v in per.items()}
 
-    # The one-shot AR+RMSNorm kernel on the same workload (forced; the default
-    # dispatch sends this size to the Lamport kernel).  Reported beside the
-    # step, not part of it.
-    ws.set_debug(are.DEBUG_AR_ONESHOT)
-    for _ in range(args.warmup):
-        are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
-    o0 = torch.cuda.Event(enable_timing=True)
-    o1 = torch.cuda.Event(enable_timing=True)
-    o0.record(stream)
-    for _ in range(args.steps):
-        are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
-    o1.record(stream)
-    torch.cuda.synchronize(dev)
-    ws.set_debug(0)
-    st = ws.device_status()
-    if st["code"] != 0:
-        raise RuntimeError(f"device status after one-shot steps: {st}")
-    oneshot_ms = max_over_ranks(dist, o0.elapsed_time(o1) / args.steps, dev)
+    # AR+RMSNorm alone, back to back: the Lamport kernel the step runs (inside the
+    # step it starts while L2 still holds GEMM+AR's output lines, whose write-back
+    # it pays for), and the one-shot kernel on the same workload (forced; the
+    # default dispatch sends this size to the Lamport kernel).  Reported beside
+    # the step, not part of it.
+    def alone(flags):
+        ws.set_debug(flags)
+        for _ in range(args.warmup):
+            are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
+        o0 = torch.cuda.Event(enable_timing=True)
+        o1 = torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        for _ in range(args.steps):
+            are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
+        o1.record(stream)
+        torch.cuda.synchronize(dev)
+        ws.set_debug(0)
+        st = ws.device_status()
+        if st["code"] != 0:
+            raise RuntimeError(f"device status after AR+RMSNorm alone ({flags}): {st}")
+        return max_over_ranks(dist, o0.elapsed_time(o1) / args.steps, dev)
+
+    lamport_alone_ms = alone(0)
+    oneshot_ms = alone(are.DEBUG_AR_ONESHOT)
 
     roof = {p: roofline_seconds(p, peaks) for p in WORKLOAD}
     value = world * 100.0 * sum(roof.values()) / (ms_step * 1e-3)
@@ -396,7 +402,10 @@ def run_gpu(args):
     roofline_ar = {"kernel": "ar_rmsnorm_kernel<4> (allreduce_rmsnorm)", "bound": "hbm", "achieved": ach_n,
                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach_n / peaks["hbm_gbs"],
                    "traffic": NCU_TRAFFIC["allreduce_rmsnorm"], "peak_source": f"{source} HBM copy",
-                   "note": f"of {source}"}
+                   "note": f"of {source}; in the step"}
+    ach_alone = bytes_n / (lamport_alone_ms * 1e-3) / 1e9
+    roofline_ar["alone"] = {"ms": lamport_alone_ms, "achieved": ach_alone, "frac": ach_alone / peaks["hbm_gbs"],
+                            "note": "the same kernel, calls back to back outside the step (inputs larger than L2)"}
 
     # ---- end to end: pinned host inputs -> device, the three calls, results -> host
     e2e_steps = max(1, min(args.steps, 5))

@@ -145,7 +145,9 @@ enum {
                               waiting for operands, [3] MMA waiting for a free accumulator, [4] MMA thread
                               from its first wait to its last commit, [5] drain waiting for an accumulator,
                               [6] loader waiting for tile masks, [7] reduce waiting for partial sub-tiles,
-                              [8] CTAs counted.  For AR+RMSNorm: [1] producer waiting for a free stage or
+                              [8] CTAs counted, and per pair, in ns of %globaltimer: [9] max and [10]
+                              sum of the time from its last MMA to its end, [11] max of its span,
+                              [12] sum of its time up to its last MMA.  For AR+RMSNorm: [1] producer waiting for a free stage or
                               residual slot, [2] phase A waiting for partials, [3] phase A held back by
                               its own phase B, [4] phase A waiting for a ring slot's re-arm, [5] phase B
                               spinning on staged words, [6] phase B waiting for its residual row, [7]

@@ -204,3 +204,32 @@ def test_ring_many_laps_repeat(oracle, M):
         assert st["code"] == 0, st
         check_close(host_f32(out), ref, f"ring M={M}")
         assert np.all(staging_words(w, M, N) == SENT)
+
+
+def test_ring_reuse_waits_for_rearm(oracle):
+    """Without re-arming, no staged word of lap 0 turns back into the lap-1
+    sentinel, so every producer's bounded check before it overwrites its row of
+    the first slot in lap 1 (chunk 8) expires: the status names that check and
+    chunk, the kernel returns, and after a reset the workspace works again."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    M, N = 4096, 1024  # more than 8 chunks of at most 2 x 152 rows: the ring laps
+    parts, res, gamma = synth.ar_inputs(2, M, N, 31)
+    P = [dev_bf16(x) for x in parts]
+    r = dev_bf16(res)
+    g = torch.from_numpy(gamma).cuda()
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with are.Workspace(R_max=8, M_max=M, N_max=N, timeout_ns=20_000_000) as w:
+        w.set_debug(are.DEBUG_NO_REARM | are.DEBUG_AR_LAMPORT)
+        are.allreduce_rmsnorm(P, r, g, 1e-6, out, w)
+        st = w.device_status()
+        assert st["status"] == are.ETIMEOUT and st["code"] == are.DEV_PIPE_TIMEOUT, st
+        assert st["a"] == -3 and st["b"] == 8, st
+        w.set_debug(0)
+        w.reset()
+        are.allreduce_rmsnorm(P, r, g, 1e-6, out, w)
+        assert w.device_status()["code"] == 0
+        check_close(host_f32(out), oracle.allreduce_rmsnorm(parts, res, gamma, 1e-6), "after reset")
+        assert np.all(staging_words(w, M, N) == SENT)

@@ -28,7 +28,8 @@ def _call_noalloc(lib, parts, res, gamma, eps, out, stream):
                                             parts[0].shape[1], stream)
 
 
-@pytest.mark.parametrize("R,M,N,resid", [(8, 64, 7168, True), (3, 5, 1000, False)])
+# 2048 x 1024 fills the array and laps the staging ring
+@pytest.mark.parametrize("R,M,N,resid", [(8, 64, 7168, True), (3, 5, 1000, False), (4, 2048, 1024, True)])
 def test_noalloc_matches_workspace_entry_point(R, M, N, resid):
     need_gpu()
     import torch
