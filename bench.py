@@ -28,6 +28,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -100,7 +101,7 @@ def roofline_seconds(part: str, peaks) -> float:
 
 # --------------------------------------------------------------------------- clocks
 
-CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -110,17 +111,23 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.path = None
+        self.window = None  # host wall-clock interval of the timed region
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            # the raw samples go to ARE_CLOCKS_DIR (default: the system temporary directory)
+            out_dir = os.environ.get("ARE_CLOCKS_DIR") or tempfile.gettempdir()
+            os.makedirs(out_dir, exist_ok=True)
+            self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={CLOCK_QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -132,24 +139,27 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), float(f[4]),
+                             {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        use, where = (inside, "timed region") if inside else (rows, "whole sampling run (no sample fell inside)")
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted(set().union(*[r[4] for r in use]))
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use), "power_w_median": statistics.median(r[3] for r in use),
+                "window": where}
 
 
 # --------------------------------------------------------------------------- distributed plumbing
@@ -197,10 +207,14 @@ def host_inputs():
 
 # --------------------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample_time(nthreads: int = 0):
+_ORACLE_INPUTS = {}
+
+
+def oracle_sample_time(nthreads: int = 0, gemm_rows: int = 64):
     """Time the oracle as it stands on bounded row samples of each part and
     extrapolate linearly in rows to one full step.  Returns (seconds per full
-    step, threads used, sample description)."""
+    step, threads used, sample description).  The synthetic operands are drawn
+    once per process (outside the timed calls)."""
     import numpy as np
 
     import oracle
@@ -209,21 +223,22 @@ def oracle_sample_time(nthreads: int = 0):
     threads = o.max_threads() if nthreads == 0 else nthreads
     total = 0.0
     desc = []
-    for part, nrows in (("gemm_rs", 64), ("gemm_ar", 64)):
+    for part, nrows in (("gemm_rs", gemm_rows), ("gemm_ar", gemm_rows)):
         w = WORKLOAD[part]
         R, M, N, K = w["R"], w["M"], w["N"], w["K"]
-        # a bounded slice of rows is enough: only those rows of A are drawn
+        # a bounded slice of rows, spread over the matrix
         rows = np.linspace(0, M - 1, nrows).astype(np.int64)
-        seed = synth.config_seed(w["seed_cfg"])
-        s = 1.0 / np.sqrt(K)
-        A = [synth.normal_bf16((M, K), seed, synth.T_A, r, 0.0, s) for r in range(R)]
-        B = [synth.normal_bf16((K, N), seed, synth.T_B, r, 0.0, s) for r in range(R)]
+        if part not in _ORACLE_INPUTS:
+            seed = synth.config_seed(w["seed_cfg"])
+            s = 1.0 / np.sqrt(K)
+            _ORACLE_INPUTS[part] = ([synth.normal_bf16((M, K), seed, synth.T_A, r, 0.0, s) for r in range(R)],
+                                    [synth.normal_bf16((K, N), seed, synth.T_B, r, 0.0, s) for r in range(R)])
+        A, B = _ORACLE_INPUTS[part]
         t0 = time.perf_counter()
         o.gemm_reduce_rows(A, B, rows, "rs" if part == "gemm_rs" else "ar")
         dt = time.perf_counter() - t0
         total += dt * M / nrows
         desc.append(f"{part}: {nrows} of {M} rows in {dt:.2f} s")
-        del A, B
     w = WORKLOAD["allreduce_rmsnorm"]
     R, M, N = w["R"], w["M"], w["N"]
     nrows = 512
@@ -242,12 +257,15 @@ def run_reference(args):
         return 0
     peaks, source = load_peaks()
     roof = sum(roofline_seconds(p, peaks) for p in WORKLOAD)
+    # each step is a row sample of the whole workload, smaller when many steps are asked
+    # for, so that the run stays within a few minutes
+    gemm_rows = max(8, min(64, (64 * 10) // max(1, args.steps)))
     for _ in range(args.warmup):
-        oracle_sample_time()
+        oracle_sample_time(gemm_rows=gemm_rows)
     times = []
     threads, sample = 0, ""
     for _ in range(args.steps):
-        t, threads, sample = oracle_sample_time()
+        t, threads, sample = oracle_sample_time(gemm_rows=gemm_rows)
         times.append(t)
     step_s = statistics.mean(times)
     value = 100.0 * roof / step_s
@@ -336,11 +354,13 @@ def run_gpu(args):
     time.sleep(0.3)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
     t_start.record(stream)
     for i in range(args.steps):
         step(events[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
+    sampler.mark(w0, time.time())
     clocks = sampler.stop()
     if dist is not None:
         dist.barrier()
@@ -532,11 +552,15 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 300 for this implementation, about a second of timed work so "
+                         "that the clock samples fall under load; 10 for --impl reference)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 10 if args.impl == "reference" else 300
     if args.warmup < 3 and args.impl == "ours":
         sys.stderr.write("note: fewer than 3 warm-up steps\n")
     if args.impl == "reference":
