@@ -214,10 +214,15 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     const bool pair_ok = tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
     if (pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA))) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
-        // GEMM+RS: run the ranks block by block (two waves of tile pairs per block) so a
-        // wave streams one or two ranks' operands; GEMM+AR keeps the ranks innermost (its
-        // reductions write R views and are better spread over the waves)
-        if (mode == kModeRS) p->block_tiles = 2 * clusters;
+        // GEMM+RS with at least three rank blocks' worth of tile pairs: run the ranks block
+        // by block (two waves of tile pairs per block) so a wave streams one or two ranks'
+        // operands.  A block's reductions all come at its end, and with fewer blocks that
+        // burst is not hidden: R=4, M=4096, N=4096, K=2048 (1.7 blocks) measured 1219 TFLOP/s
+        // with the ranks innermost against 1097 rank-blocked; M=8192 (3.5 blocks) 1323
+        // against 1360.  GEMM+AR keeps the ranks innermost (its reductions write R views and
+        // are better spread over the waves).
+        const int64_t rs_block = 2 * (int64_t)clusters;
+        if (mode == kModeRS && (int64_t)p->pairs_m * tiles_n >= 3 * rs_block) p->block_tiles = (int)rs_block;
         if (p->block_tiles > 0) {
             const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
             const int64_t blocks = (num_pairs + p->block_tiles - 1) / p->block_tiles;
