@@ -377,10 +377,9 @@ def run_gpu(args):
     per_ms = {p: statistics.mean(v) for p, v in per.items()}
 
     # AR+RMSNorm alone, back to back: the Lamport kernel the step runs (inside the
-    # step it runs at the SM clock the power cap leaves while the GEMMs run, and
-    # it is latency-bound), and the one-shot kernel on the same workload (forced;
-    # the default dispatch sends this size to the Lamport kernel).  Reported
-    # beside the step, not part of it.
+    # step it runs at the clock the power cap leaves while the GEMMs run), and the
+    # one-shot kernel on the same workload (forced; the default dispatch sends this
+    # size to the Lamport kernel).  Reported beside the step, not part of it.
     def alone(flags):
         ws.set_debug(flags)
         for _ in range(args.warmup):
