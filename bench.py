@@ -517,6 +517,10 @@ def run_gpu(args):
         cpu_s, threads, sample = oracle_sample_time()
         cpu = {"value": 100.0 * sum(roof.values()) / cpu_s, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": sample, "ms_per_step_extrapolated": cpu_s * 1e3}
+        # the same oracle on one thread, on a smaller row sample
+        cpu1_s, _, sample1 = oracle_sample_time(nthreads=1, gemm_rows=8)
+        cpu["single_thread"] = {"value": 100.0 * sum(roof.values()) / cpu1_s, "cores": 1, "sample": sample1,
+                                "ms_per_step_extrapolated": cpu1_s * 1e3}
 
     if rank == 0:
         line = {
