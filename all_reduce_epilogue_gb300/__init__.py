@@ -24,7 +24,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libare.so")
 
 # status codes (are_status)
-OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBUSY, ENODEV, ECAPACITY = range(8)
+OK, EINVAL, ENOMEM, ECUDA, ETIMEOUT, EBUSY, ENODEV, ECAPACITY, ECAPTURE = range(9)
 # ops
 OP_GEMM_RS, OP_GEMM_AR, OP_ALLREDUCE_RMSNORM = 1, 2, 3
 # debug flags
@@ -34,6 +34,9 @@ DEBUG_SINGLE_CTA, DEBUG_WAIT_PROFILE, DEBUG_AR_ONESHOT, DEBUG_AR_LAMPORT, DEBUG_
 DEV_OK, DEV_MASK_TIMEOUT, DEV_STAGE_TIMEOUT, DEV_PIPE_TIMEOUT = 0, 1, 2, 3
 # snapshot kinds
 SNAP_MASKS, SNAP_STAGING, SNAP_PIECES, SNAP_COUNTERS = 1, 2, 3, 4
+# kernels (are_kernel), as reported by Workspace.last_launch()
+KERNEL_NAMES = {0: "none", 1: "memset", 2: "gemm_reduce_kernel", 3: "gemm_pair_kernel", 4: "ar_rmsnorm_kernel",
+                5: "ar_oneshot_kernel"}
 PIECE_WORDS = 64
 TILE_M, TILE_N = 128, 256
 
@@ -41,9 +44,9 @@ TILE_M, TILE_N = 128, 256
 EXPORTS = [
     "are_version", "are_status_string", "are_supports", "are_workspace_create", "are_workspace_destroy",
     "are_workspace_reset", "are_workspace_set_debug", "are_workspace_set_oneshot_max_bytes",
-    "are_get_device_status", "are_debug_snapshot",
+    "are_get_device_status", "are_debug_snapshot", "are_debug_last_launch",
     "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_add_rmsnorm", "are_allreduce_rmsnorm_quant",
-    "are_allreduce_rmsnorm_noalloc",
+    "are_allreduce_rmsnorm_noalloc", "are_noalloc_device_status",
 ]
 
 
@@ -65,6 +68,12 @@ class _Caps(ctypes.Structure):
 
 class _DevStatus(ctypes.Structure):
     _fields_ = [("code", ctypes.c_uint32), ("where", ctypes.c_uint32), ("a", ctypes.c_int32), ("b", ctypes.c_int32)]
+
+
+class _LaunchInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("grid", ctypes.c_int32), ("block", ctypes.c_int32),
+                ("cluster", ctypes.c_int32), ("rank_block", ctypes.c_int32), ("variant", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lib = None
@@ -100,6 +109,10 @@ def load_library(path: str = LIB_PATH):
     lib.are_get_device_status.argtypes = [vp, ctypes.POINTER(_DevStatus)]
     lib.are_debug_snapshot.restype = i32
     lib.are_debug_snapshot.argtypes = [vp, i32, vp, ctypes.c_size_t]
+    lib.are_debug_last_launch.restype = i32
+    lib.are_debug_last_launch.argtypes = [vp, ctypes.POINTER(_LaunchInfo)]
+    lib.are_noalloc_device_status.restype = i32
+    lib.are_noalloc_device_status.argtypes = [ctypes.POINTER(_DevStatus)]
     for name in ("are_gemm_rs", "are_gemm_ar"):
         f = getattr(lib, name)
         f.restype = i32
@@ -208,6 +221,14 @@ class Workspace:
         if rc not in (OK, ETIMEOUT):
             raise AreError(rc, "are_get_device_status")
         return {"status": rc, "code": st.code, "where": st.where, "a": st.a, "b": st.b}
+
+    def last_launch(self) -> dict:
+        """Which kernel the last operation on this workspace launched, and its
+        launch shape (host-side record; no device access)."""
+        li = _LaunchInfo()
+        _check(load_library().are_debug_last_launch(self.handle, ctypes.byref(li)), "are_debug_last_launch")
+        return {"kernel": KERNEL_NAMES.get(li.kernel, str(li.kernel)), "grid": li.grid, "block": li.block,
+                "cluster": li.cluster, "rank_block": li.rank_block, "variant": li.variant}
 
     def snapshot(self, kind: int, nbytes: int):
         import numpy as np
@@ -342,3 +363,13 @@ def allreduce_rmsnorm_noalloc(partials: Sequence, residual, gamma, eps: float, o
         _ptrs(partials), residual.data_ptr() if residual is not None else None, gamma.data_ptr(), float(eps),
         out.data_ptr(), R, M, N, _stream_handle(stream))
     _check(rc, "are_allreduce_rmsnorm_noalloc")
+
+
+def noalloc_device_status() -> dict:
+    """Status word of the allocation-free entry point on the current device
+    (synchronises the device; describes the last call only)."""
+    st = _DevStatus()
+    rc = load_library().are_noalloc_device_status(ctypes.byref(st))
+    if rc not in (OK, ETIMEOUT):
+        raise AreError(rc, "are_noalloc_device_status")
+    return {"status": rc, "code": st.code, "where": st.where, "a": st.a, "b": st.b}

@@ -42,6 +42,8 @@ struct are_ws {
     int64_t debug_arg = -1;
     uint64_t timeout_ns = 0;
     int64_t last_ar_M = 0, last_ar_N = 0;
+    int pair_clusters = 0;            // co-resident clusters of the pair kernel on `device`
+    are_launch_info last{};           // what the last operation launched
 };
 
 namespace {
@@ -131,6 +133,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     const int64_t T = tiles_m * tiles_n;
     if ((size_t)T > ws->mask_words || (size_t)(R * T) * kTilePartBytes > ws->part_bytes) return ARE_ECAPACITY;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    ws->last = are_launch_info{};
     if (M == 0 || N == 0) return ARE_OK;
 
     // distinct output views (GEMM+AR views may alias)
@@ -144,6 +147,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         }
     }
     if (K == 0) {  // empty contraction: the result is zero
+        ws->last.kernel = ARE_KERNEL_MEMSET;
         if (mode == kModeRS) {
             for (int r = 0; r < R; ++r) {
                 cudaError_t e = cudaMemsetAsync(out[r], 0, (size_t)(M / R) * N * 2, s);
@@ -206,7 +210,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     p->timeout_ns = ws->timeout_ns;
     // CTA pairs (256-row tiles) wherever there are at least two tile rows and
     // the device can co-schedule the clusters; one CTA per tile otherwise.
-    const int clusters = gemm_pair_max_clusters();
+    const int clusters = ws->pair_clusters;
     // Below one wave of pairs the reduce of the last (only) wave is the kernel's tail, and
     // the one-CTA kernel's deeper partial buffer (and its reducer's own partial kept in
     // TMEM) finishes it sooner: R=4, M=256 measured 33 us against 69 us.
@@ -229,10 +233,12 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
             p->num_pair_units = (int)(blocks * p->block_tiles * R);
         }
         const int grid = 2 * (int)std::min<int64_t>(p->num_pair_units, clusters);
+        ws->last = are_launch_info{ARE_KERNEL_GEMM_PAIR, grid, gemm_pair_threads(), 2, p->block_tiles, 0, {0, 0}};
         e = launch_gemm_pair(*p, mode, grid, s);
     } else {
         p->group_m = (int)std::min<int64_t>(tiles_m, 8);
         const int grid = (int)std::min<int64_t>(p->num_units, ws->num_sms);
+        ws->last = are_launch_info{ARE_KERNEL_GEMM_ONE_CTA, grid, kGemmThreads, 1, 0, 0, {0, 0}};
         e = launch_gemm_reduce(*p, mode, grid, s);
     }
     delete p;
@@ -255,6 +261,7 @@ const char* are_status_string(are_status s) {
         case ARE_EBUSY: return "ARE_EBUSY: workspace in use by another thread";
         case ARE_ENODEV: return "ARE_ENODEV: current device is not sm_103";
         case ARE_ECAPACITY: return "ARE_ECAPACITY: call exceeds workspace capacity";
+        case ARE_ECAPTURE: return "ARE_ECAPTURE: one-time set-up needed inside a stream capture";
     }
     return "unknown are_status";
 }
@@ -312,6 +319,7 @@ are_status are_workspace_create(are_ws** out, const are_caps* caps) {
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_part, ws->part_bytes);
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_pieces, ws->piece_words * 4);
         if (e == cudaSuccess) e = gemm_prepare_kernels();
+        if (e == cudaSuccess) ws->pair_clusters = gemm_pair_max_clusters();
     }
     if (e == cudaSuccess && caps->N_max <= 32768) {
         ws->staging_words = (size_t)caps->M_max * (size_t)caps->N_max;
@@ -382,6 +390,14 @@ are_status are_get_device_status(are_ws* ws, are_dev_status* out) {
     return d.code == ARE_DEV_OK ? ARE_OK : ARE_ETIMEOUT;
 }
 
+are_status are_debug_last_launch(are_ws* ws, are_launch_info* out) {
+    if (!ws || !out) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    *out = ws->last;
+    return ARE_OK;
+}
+
 are_status are_debug_snapshot(are_ws* ws, int kind, void* host_dst, size_t bytes) {
     if (!ws || !host_dst) return ARE_EINVAL;
     const void* src = nullptr;
@@ -431,6 +447,7 @@ are_status allreduce_rmsnorm_call(const are_bf16* const partials[], const are_bf
     if (R > ws->caps.R_max || M > ws->caps.M_max || N > ws->caps.N_max || !ws->d_staging ||
         (size_t)M * (size_t)N > ws->staging_words)
         return ARE_ECAPACITY;
+    ws->last = are_launch_info{};
     if (M == 0 || N == 0) return ARE_OK;
 
     ArParams p;
@@ -472,8 +489,10 @@ are_status allreduce_rmsnorm_call(const are_bf16* const partials[], const are_bf
                          ((ws->debug_flags & ARE_DEBUG_AR_ONESHOT) || (uint64_t)M * (uint64_t)N * 2 <= ws->oneshot_max_bytes);
     if (oneshot) {
         const int os_grid = (int)std::min<int64_t>(M, ws->num_sms);
+        ws->last = are_launch_info{ARE_KERNEL_AR_ONESHOT, os_grid, ar_oneshot_threads(), 1, 0, ppt, {0, 0}};
         return from_cuda(launch_ar_oneshot(p, ppt, os_grid, s));
     }
+    ws->last = are_launch_info{ARE_KERNEL_AR_LAMPORT, grid, kArThreads, 1, 0, ppt, {0, 0}};
     return from_cuda(launch_ar_rmsnorm(p, ppt, grid, s));
 }
 

@@ -811,6 +811,8 @@ cudaError_t ar_oneshot_prepare() {
     return e;
 }
 
+int ar_oneshot_threads() { return kOsThreads; }
+
 cudaError_t launch_ar_oneshot(const ArParams& p, int ppt, int grid, cudaStream_t stream) {
     const size_t smem = ar_oneshot_smem_bytes(p.R, p.N, p.residual != nullptr);
     switch (ppt) {

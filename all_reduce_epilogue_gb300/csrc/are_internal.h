@@ -74,6 +74,7 @@ size_t ar_oneshot_smem_bytes(int R, int N, bool residual);
 bool ar_oneshot_fits(int R, int N, bool residual);
 cudaError_t ar_oneshot_prepare();
 cudaError_t launch_ar_oneshot(const ArParams& p, int ppt, int grid, cudaStream_t stream);
+int ar_oneshot_threads();
 // Fill n 32-bit words with v.
 cudaError_t launch_fill_u32(uint32_t* dst, uint32_t v, size_t n, cudaStream_t stream);
 
@@ -122,7 +123,9 @@ cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uin
 cudaError_t launch_gemm_reduce(const GemmParams& p, int mode, int grid, cudaStream_t stream);
 // CTA-pair variant (cta_group::2 UMMA, 256x256 per pair); grid = 2 x clusters.
 cudaError_t launch_gemm_pair(const GemmParams& p, int mode, int grid, cudaStream_t stream);
-// Largest number of co-resident 2-CTA clusters of the pair kernel (0 if unavailable).
+// Largest number of co-resident 2-CTA clusters of the pair kernel on the current
+// device (0 if unavailable); valid after gemm_prepare_kernels() on that device.
 int gemm_pair_max_clusters();
+int gemm_pair_threads();
 
 }  // namespace are

@@ -1184,7 +1184,11 @@ cudaError_t get_encode() {
 
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
-int g_pair_clusters = -1;
+// Co-resident clusters of the pair kernel, per device (-1 = not yet queried).
+constexpr int kMaxDevices = 64;
+std::mutex g_pair_mu;
+int g_pair_clusters[kMaxDevices];
+bool g_pair_init = false;
 
 cudaLaunchConfig_t pair_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
@@ -1214,20 +1218,38 @@ cudaError_t gemm_prepare_kernels() {
     e = cudaFuncSetAttribute(gemm_pair_kernel<kModeAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes2);
     if (e != cudaSuccess) return e;
-    if (g_pair_clusters < 0) {
-        // co-resident clusters bound the persistent grid (every cluster must be running)
-        int n_rs = 0, n_ar = 0;
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg = pair_config(2 * 1024, nullptr, attr);
-        if (cudaOccupancyMaxActiveClusters(&n_rs, (void*)gemm_pair_kernel<kModeRS>, &cfg) != cudaSuccess) n_rs = 0;
-        if (cudaOccupancyMaxActiveClusters(&n_ar, (void*)gemm_pair_kernel<kModeAR>, &cfg) != cudaSuccess) n_ar = 0;
-        cudaGetLastError();
-        g_pair_clusters = n_rs < n_ar ? n_rs : n_ar;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lk(g_pair_mu);
+        if (!g_pair_init) {
+            for (int d = 0; d < kMaxDevices; ++d) g_pair_clusters[d] = -1;
+            g_pair_init = true;
+        }
+        if (g_pair_clusters[dev] < 0) {
+            // co-resident clusters bound the persistent grid (every cluster must be running)
+            int n_rs = 0, n_ar = 0;
+            cudaLaunchAttribute attr[1];
+            cudaLaunchConfig_t cfg = pair_config(2 * 1024, nullptr, attr);
+            if (cudaOccupancyMaxActiveClusters(&n_rs, (void*)gemm_pair_kernel<kModeRS>, &cfg) != cudaSuccess) n_rs = 0;
+            if (cudaOccupancyMaxActiveClusters(&n_ar, (void*)gemm_pair_kernel<kModeAR>, &cfg) != cudaSuccess) n_ar = 0;
+            cudaGetLastError();
+            g_pair_clusters[dev] = n_rs < n_ar ? n_rs : n_ar;
+        }
     }
     return get_encode();
 }
 
-int gemm_pair_max_clusters() { return g_pair_clusters < 0 ? 0 : g_pair_clusters; }
+int gemm_pair_max_clusters() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_pair_mu);
+    return (g_pair_init && g_pair_clusters[dev] > 0) ? g_pair_clusters[dev] : 0;
+}
+
+int gemm_pair_threads() { return kPairThreads; }
 
 // bf16 [outer, inner] row-major, 128B-swizzled boxes of box_inner x box_outer.
 cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,

@@ -41,13 +41,19 @@ std::mutex g_mu;
 DeviceScratch g_devices[kMaxDevices];
 
 // Once per device, with that device current: look up the array's device
-// address and the kernel's co-resident grid limits.
-are_status setup_current_device(DeviceScratch** out) {
+// address and the kernel's co-resident grid limits.  These runtime queries may
+// not run while `stream` is being captured into a graph (a capture in global
+// mode would be invalidated), so a first call made under capture is refused
+// before it queries anything.
+are_status setup_current_device(DeviceScratch** out, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ARE_ENODEV;
     std::lock_guard<std::mutex> lk(g_mu);
     DeviceScratch& d = g_devices[dev];
     if (d.base == nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return ARE_ECUDA;
+        if (cs != cudaStreamCaptureStatusNone) return ARE_ECAPTURE;
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -85,8 +91,9 @@ extern "C" are_status are_allreduce_rmsnorm_noalloc(const are_bf16* const partia
     if ((size_t)M * (size_t)N > kStagingWords) return ARE_ECAPACITY;
     if (M == 0 || N == 0) return ARE_OK;
 
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     DeviceScratch* d = nullptr;
-    st = setup_current_device(&d);
+    st = setup_current_device(&d, s);
     if (st != ARE_OK) return st;
 
     ArParams p;
@@ -119,9 +126,24 @@ extern "C" are_status are_allreduce_rmsnorm_noalloc(const are_bf16* const partia
     // The array keeps the previous call's contents: clear the status word and
     // arm the staging words this call uses with the -0.0 sentinel, so a call
     // never depends on how the one before it ended.
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(d->base, 0, kHeaderWords * sizeof(uint32_t), s);
     if (e == cudaSuccess) e = launch_fill_u32(p.staging, kSentinelF32, (size_t)M * (size_t)N, s);
     if (e == cudaSuccess) e = launch_ar_rmsnorm(p, ppt, grid, s);
     return e == cudaSuccess ? ARE_OK : ARE_ECUDA;
+}
+
+extern "C" are_status are_noalloc_device_status(are_dev_status* out) {
+    if (!out) return ARE_EINVAL;
+    DeviceScratch* d = nullptr;
+    are_status st = setup_current_device(&d, nullptr);
+    if (st != ARE_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    DevStatus v{};
+    if (e == cudaSuccess) e = cudaMemcpy(&v, d->base, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return ARE_ECUDA;
+    out->code = v.code;
+    out->where = v.where;
+    out->a = v.a;
+    out->b = v.b;
+    return v.code == ARE_DEV_OK ? ARE_OK : ARE_ETIMEOUT;
 }

@@ -14,12 +14,17 @@ Every input is larger than the 129 MB L2, so no flush is needed between
 steps.  ``value`` is the step's roofline fraction: the sum over the three
 kernels of max(FLOPs / bf16 peak, algorithmic bytes / HBM bandwidth),
 divided by the measured step time (per GPU; summed over GPUs for N > 1,
-where every rank runs its own replica).
+where every rank runs its own replica).  The bf16 peak is the burst figure
+when the clock samples of the timed region show the SM clock at its maximum
+with no power capping, the sustained figure otherwise.
+
+After the step, ``configs`` times every workload at every size one by one
+(CUDA graphs of calls), with the kernel each call launched.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 ``--impl reference`` times the CPU oracle (the only reference implementation
-that exists for this method) on bounded row samples of the same workload.
+that exists for this method) on one bounded sample of the workload per step.
 """
 from __future__ import annotations
 
@@ -44,28 +49,56 @@ WORKLOAD = {
     "allreduce_rmsnorm": dict(R=8, M=4096, N=7168, seed_cfg=3),
 }
 EPS = 1e-6
+L2_BYTES = 129e6
 # Fallback denominators (one earlier GB300 measurement), used only when the
 # measured peaks file is absent.
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
-# each part's kernel at this workload, from one ncu capture of a bench step
-# (profiles/launch_list_bench_step.md).  Set back to None whenever that kernel's
-# source changes, until it is captured again.
-NCU_TRAFFIC = {"gemm_rs": 9935.3e6, "gemm_ar": 3557.5e6, "allreduce_rmsnorm": 639.2e6}
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# part's kernel at this workload, from one ncu capture, keyed to the SHA-256
+# (first 16 hex digits) of the kernel's source file at capture time: when the
+# source has changed since, the figure no longer describes the kernel and the
+# line reports null.
+KERNEL_SOURCES = {"gemm_rs": "gemm_reduce.cu", "gemm_ar": "gemm_reduce.cu", "allreduce_rmsnorm": "ar_rmsnorm.cu"}
+NCU_TRAFFIC = {
+    "gemm_rs": (None, None),
+    "gemm_ar": (None, None),
+    "allreduce_rmsnorm": (None, None),
+}
+
+
+def source_sha16(name: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, "all_reduce_epilogue_gb300", "csrc", name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def ncu_traffic(part: str):
+    val, sha = NCU_TRAFFIC[part]
+    if val is None or sha != source_sha16(KERNEL_SOURCES[part]):
+        return None
+    return val
 
 
 # --------------------------------------------------------------------------- work model
 
+def work_of(op: str, R: int, M: int, N: int, K: int = 0, residual: bool = True):
+    """(FLOPs, algorithmic bytes) of one call.  GEMMs: 2RMNK; bytes = the R
+    operand pairs read once plus the output written once (GEMM+AR: R views).
+    AR+RMSNorm: R partial rows + the residual row read, the output row
+    written, gamma read once."""
+    if op == "allreduce_rmsnorm":
+        return 0.0, float(2 * M * N * (R + (2 if residual else 1)) + 4 * N)
+    flops = 2.0 * R * M * N * K
+    if op == "gemm_rs":
+        return flops, float(2 * (R * M * K + R * K * N + M * N))
+    if op == "gemm_ar":
+        return flops, float(2 * (R * M * K + R * K * N + R * M * N))
+    raise ValueError(op)
+
+
 def work(part: str):
     w = WORKLOAD[part]
-    R, M, N = w["R"], w["M"], w["N"]
-    if part == "allreduce_rmsnorm":
-        return 0.0, float(2 * M * N * (R + 2) + 4 * N)
-    K = w["K"]
-    flops = 2.0 * R * M * N * K
-    if part == "gemm_rs":
-        return flops, float(2 * (R * M * K + R * K * N + M * N))
-    return flops, float(2 * (R * M * K + R * K * N + R * M * N))
+    return work_of(part, w["R"], w["M"], w["N"], w.get("K", 0))
 
 
 def load_peaks():
@@ -94,9 +127,31 @@ def load_peaks():
     return peaks, source
 
 
-def roofline_seconds(part: str, peaks) -> float:
-    flops, byts = work(part)
-    return max(flops / (peaks["bf16_tflops_sustained"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+def bf16_peak(peaks, regime: str) -> float:
+    return peaks["bf16_tflops"] if regime == "burst" else peaks["bf16_tflops_sustained"]
+
+
+def roofline_seconds_of(flops: float, byts: float, peaks, regime: str) -> float:
+    return max(flops / (bf16_peak(peaks, regime) * 1e12), byts / (peaks["hbm_gbs"] * 1e9))
+
+
+def roofline_seconds(part: str, peaks, regime: str = "burst") -> float:
+    return roofline_seconds_of(*work(part), peaks, regime)
+
+
+def peak_regime(clocks) -> tuple:
+    """Which bf16 peak the timed region ran under: 'burst' (the GEMM peak timed
+    alone) when its clock samples show the SM clock at (or within 3% of) its
+    maximum and no power capping, 'sustained' (the seconds-long figure under
+    the power cap) when the power cap was active or the clock sat lower.  With
+    no sample inside the region the burst peak is taken: the higher
+    denominator, so the fraction is not overstated."""
+    sm, smax, reasons = clocks.get("sm_mhz"), clocks.get("sm_max_mhz"), clocks.get("reasons") or []
+    if clocks.get("window") != "timed region" or not sm or not smax:
+        return "burst", "no clock sample inside the timed region: burst peak (the larger denominator)"
+    if "sw_power_cap" in reasons or sm < 0.97 * smax:
+        return "sustained", f"median SM clock {sm:.0f} of {smax:.0f} MHz, reasons {reasons}: sustained peak"
+    return "burst", f"median SM clock {sm:.0f} of {smax:.0f} MHz, no power capping: burst peak"
 
 
 # --------------------------------------------------------------------------- clocks
@@ -104,14 +159,19 @@ def roofline_seconds(part: str, peaks) -> float:
 CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+CLOCK_PERIOD_MS = 20
 
 
 class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every CLOCK_PERIOD_MS, read
+    back per host wall-clock window (the timed region, the per-workload
+    timings)."""
+
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
         self.path = None
-        self.window = None  # host wall-clock interval of the timed region
+        self.rows = None
 
     def start(self):
         try:
@@ -121,18 +181,15 @@ class ClockSampler:
             self.path = os.path.join(out_dir, f"clocks_bench_{os.getpid()}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={CLOCK_QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(CLOCK_PERIOD_MS)],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
-    def mark(self, t0: float, t1: float):
-        self.window = (t0, t1)
-
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+            return
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -141,25 +198,31 @@ class ClockSampler:
         self.fh.close()
         import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        rows = []
+        self.rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
             if len(f) < 10:
                 continue
             try:
                 ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append((ts, float(f[2]), float(f[3]), float(f[4]),
-                             {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
+                self.rows.append((ts, float(f[2]), float(f[3]), float(f[4]),
+                                  {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
             except ValueError:
                 continue
-        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
-        use, where = (inside, "timed region") if inside else (rows, "whole sampling run (no sample fell inside)")
+
+    def summary(self, window) -> dict:
+        """Median SM clock, maximum clock, power and the throttle reasons of the
+        samples inside `window` (host wall-clock seconds)."""
+        if self.proc is None or self.rows is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "window": "none"}
+        inside = [r for r in self.rows if window[0] <= r[0] <= window[1]]
+        use, where = (inside, "timed region") if inside else (self.rows, "whole sampling run (no sample fell inside)")
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "window": "none"}
         reasons = sorted(set().union(*[r[4] for r in use]))
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
                 "reasons": reasons, "samples": len(use), "power_w_median": statistics.median(r[3] for r in use),
-                "window": where}
+                "period_ms": CLOCK_PERIOD_MS, "window": where}
 
 
 # --------------------------------------------------------------------------- distributed plumbing
@@ -210,24 +273,27 @@ def host_inputs():
 _ORACLE_INPUTS = {}
 
 
-def oracle_sample_time(nthreads: int = 0, gemm_rows: int = 64):
-    """Time the oracle as it stands on bounded row samples of each part and
-    extrapolate linearly in rows to one full step.  Returns (seconds per full
-    step, threads used, sample description).  The synthetic operands are drawn
-    once per process (outside the timed calls)."""
+def oracle_sample_step(nthreads: int = 0, gemm_rows: int = 64):
+    """Time the oracle as it stands on one bounded sample of the step: `gemm_rows`
+    rows (spread over the matrix, every rank, full N and K) of each GEMM part
+    and all rows of the AR+RMSNorm part.  Returns a dict: the measured seconds
+    of the sample, the sampled fraction of each part's rows, the full step's
+    time extrapolated linearly in rows, threads used and a description.  The
+    synthetic operands are drawn once per process (outside the timed calls)."""
     import numpy as np
 
     import oracle
     import synth
     o = oracle.Oracle(0, nthreads)
     threads = o.max_threads() if nthreads == 0 else nthreads
-    total = 0.0
+    measured = 0.0
+    full = 0.0
+    frac = {}
     desc = []
-    for part, nrows in (("gemm_rs", gemm_rows), ("gemm_ar", gemm_rows)):
+    for part in ("gemm_rs", "gemm_ar"):
         w = WORKLOAD[part]
         R, M, N, K = w["R"], w["M"], w["N"], w["K"]
-        # a bounded slice of rows, spread over the matrix
-        rows = np.linspace(0, M - 1, nrows).astype(np.int64)
+        rows = np.linspace(0, M - 1, gemm_rows).astype(np.int64)
         if part not in _ORACLE_INPUTS:
             seed = synth.config_seed(w["seed_cfg"])
             s = 1.0 / np.sqrt(K)
@@ -237,46 +303,63 @@ def oracle_sample_time(nthreads: int = 0, gemm_rows: int = 64):
         t0 = time.perf_counter()
         o.gemm_reduce_rows(A, B, rows, "rs" if part == "gemm_rs" else "ar")
         dt = time.perf_counter() - t0
-        total += dt * M / nrows
-        desc.append(f"{part}: {nrows} of {M} rows in {dt:.2f} s")
+        measured += dt
+        full += dt * M / gemm_rows
+        frac[part] = gemm_rows / M
+        desc.append(f"{part}: {gemm_rows} of {M} rows in {dt:.2f} s")
     w = WORKLOAD["allreduce_rmsnorm"]
     R, M, N = w["R"], w["M"], w["N"]
-    nrows = 512
-    parts, res, gamma = synth.ar_inputs(R, nrows, N, synth.config_seed(w["seed_cfg"]))
+    if "allreduce_rmsnorm" not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS["allreduce_rmsnorm"] = synth.ar_inputs(R, M, N, synth.config_seed(w["seed_cfg"]))
+    parts, res, gamma = _ORACLE_INPUTS["allreduce_rmsnorm"]
     t0 = time.perf_counter()
     o.allreduce_rmsnorm(parts, res, gamma, EPS)
     dt = time.perf_counter() - t0
-    total += dt * M / nrows
-    desc.append(f"allreduce_rmsnorm: {nrows} of {M} rows in {dt:.3f} s")
-    return total, threads, "; ".join(desc) + "; extrapolated linearly in rows to one full step"
+    measured += dt
+    full += dt
+    frac["allreduce_rmsnorm"] = 1.0
+    desc.append(f"allreduce_rmsnorm: all {M} rows in {dt:.3f} s")
+    return {"seconds": measured, "full_step_seconds_extrapolated": full, "fraction": frac, "threads": threads,
+            "sample": "; ".join(desc)}
+
+
+def sample_roofline_seconds(frac, peaks, regime="burst") -> float:
+    """Roofline time of the sampled work: each part's roofline time scaled by
+    the fraction of its rows in the sample (the GEMMs' work is linear in rows)."""
+    return sum(roofline_seconds(p, peaks, regime) * frac[p] for p in WORKLOAD)
 
 
 def run_reference(args):
+    """The reference arm: the oracle on the host cores.  Each step is one bounded
+    sample of the workload (a row sample of each GEMM, all rows of AR+RMSNorm);
+    ms_per_step is the measured time of that sample, and value is the oracle's
+    throughput on it as a fraction of the roofline of the same sampled work."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     peaks, source = load_peaks()
-    roof = sum(roofline_seconds(p, peaks) for p in WORKLOAD)
-    # each step is a row sample of the whole workload, smaller when many steps are asked
-    # for, so that the run stays within a few minutes
+    # smaller row samples when many steps are asked for, so that the run stays
+    # within a few minutes
     gemm_rows = max(8, min(64, (64 * 10) // max(1, args.steps)))
     for _ in range(args.warmup):
-        oracle_sample_time(gemm_rows=gemm_rows)
-    times = []
-    threads, sample = 0, ""
-    for _ in range(args.steps):
-        t, threads, sample = oracle_sample_time(gemm_rows=gemm_rows)
-        times.append(t)
-    step_s = statistics.mean(times)
+        oracle_sample_step(gemm_rows=gemm_rows)
+    runs = [oracle_sample_step(gemm_rows=gemm_rows) for _ in range(args.steps)]
+    step_s = statistics.mean(r["seconds"] for r in runs)
+    roof = sample_roofline_seconds(runs[0]["fraction"], peaks)
     value = 100.0 * roof / step_s
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": config_block(),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "step": f"one bounded sample of the workload per step: {runs[0]['sample']}",
+        "ms_per_step_full_extrapolated": statistics.mean(r["full_step_seconds_extrapolated"] for r in runs) * 1e3,
+        "extrapolation": "ms_per_step_full_extrapolated scales each GEMM part's measured time by M / sampled rows; "
+                         "value and ms_per_step are measured on the sample, not extrapolated",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": runs[0]["threads"], "kind": "oracle",
+                         "sample": runs[0]["sample"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "peaks": {"source": source, **peaks},
+        "peaks": {"source": source, "regime": "burst", **peaks},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -288,6 +371,173 @@ def config_block():
             "parts": {k: {kk: vv for kk, vv in v.items() if kk != "seed_cfg"} for k, v in WORKLOAD.items()},
             "parallelism": "replicas (one full step per GPU; the ranks are emulated on each GPU)",
             "l2": "inputs larger than L2 (each part streams >= 369 MB), no flush"}
+
+
+# --------------------------------------------------------------------------- every workload, one by one
+
+# (name, op, R, M list, N, K, seed config, input distribution)
+CONFIGS = [
+    ("tiny gemm_rs + rmsnorm", "gemm_rs_rmsnorm", 2, [64], 256, 128, 0, "uniform"),
+    ("gemm_rs R=4", "gemm_rs", 4, [256, 1024, 4096, 8192], 4096, 2048, 1, "normal"),
+    ("gemm_ar R=8", "gemm_ar", 8, [64, 512, 4096], 7168, 2048, 2, "normal"),
+    ("allreduce_rmsnorm R=8", "allreduce_rmsnorm", 8, [1, 16, 128, 1024, 4096], 7168, 0, 3, "normal"),
+    ("large gemm_rs R=8", "gemm_rs", 8, [8192], 8192, 4096, 4, "normal"),
+]
+
+
+def time_calls(calls, dev, replays: int = 3):
+    """Capture the callables `calls` (one library call each, on the current
+    stream) in one CUDA graph, replay it once untimed, then `replays` times
+    timed with CUDA events on the replay stream.  Returns the per-call times
+    (us) of the replays."""
+    import torch
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        for c in calls[:2]:
+            c()  # outside the capture once (lazy set-up)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for c in calls:
+            c()
+    cur = torch.cuda.current_stream(dev)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    out = []
+    for _ in range(replays):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize(dev)
+        out.append(e0.elapsed_time(e1) * 1e3 / len(calls))
+    del g
+    return out
+
+
+def run_configs(ws, dev, dev_step, peaks, sampler_windows):
+    """Every workload at every size: microseconds per call (CUDA graph of
+    calls, median and best of 3 replays), throughput, the roofline fraction at
+    the burst and sustained bf16 peaks, and which kernel ran.  Inputs are
+    rotated over enough copies that the calls of one replay stream at least
+    twice the L2 size (no L2 flush is needed)."""
+    import numpy as np
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    import synth
+
+    def to_dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    results = []
+    for name, op, R, Ms, N, K, cfg, dist_name in CONFIGS:
+        seed = synth.config_seed(cfg)
+        Mmax = max(Ms)
+        # inputs at the largest size (row prefixes give the smaller ones)
+        if op == "allreduce_rmsnorm":
+            if Mmax == WORKLOAD["allreduce_rmsnorm"]["M"] and cfg == WORKLOAD["allreduce_rmsnorm"]["seed_cfg"]:
+                P_full, res_full, gamma_d = dev_step["allreduce_rmsnorm"]
+            else:
+                ph, rh, gh = synth.ar_inputs(R, Mmax, N, seed)
+                P_full, res_full, gamma_d = [to_dev(x) for x in ph], to_dev(rh), torch.from_numpy(gh).to(dev)
+        else:
+            key = "gemm_rs" if (op == "gemm_rs" and R == 8) else ("gemm_ar" if op == "gemm_ar" else None)
+            if key and WORKLOAD[key]["M"] == Mmax and WORKLOAD[key]["seed_cfg"] == cfg:
+                A_full, B_full = dev_step[key]
+            else:
+                Ah, Bh = synth.gemm_inputs(R, Mmax, N, K, seed, dist=dist_name)
+                A_full, B_full = [to_dev(a) for a in Ah], [to_dev(b) for b in Bh]
+            if op == "gemm_rs_rmsnorm":
+                gamma_d = torch.from_numpy(synth.normal_f32((N,), seed, synth.T_GAMMA, 0, 1.0, 0.1)).to(dev)
+        paths = ["default", "oneshot", "lamport"] if op == "allreduce_rmsnorm" else ["default"]
+        for M in Ms:
+            if op == "gemm_rs_rmsnorm":
+                flops, byts = work_of("gemm_rs", R, M, N, K)
+                f2, b2 = work_of("allreduce_rmsnorm", 1, M, N, residual=False)
+                flops, byts = flops + f2, byts + b2
+            elif op == "allreduce_rmsnorm":
+                flops, byts = work_of(op, R, M, N)
+            else:
+                flops, byts = work_of(op, R, M, N, K)
+            n_sets = int(min(1024, max(1, -(-2 * L2_BYTES // byts))))
+            n_calls = max(n_sets, 20 if flops < 1e12 else 10)
+            sets = []
+            for k in range(n_sets):
+                cp = (lambda t: t) if k == 0 else (lambda t: t.clone())
+                if op == "allreduce_rmsnorm":
+                    sets.append(([cp(x[:M]) for x in P_full], cp(res_full[:M]),
+                                 torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+                elif op == "gemm_ar":
+                    sets.append(([cp(a[:M]) for a in A_full], [cp(b) for b in B_full],
+                                 [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(R)]))
+                else:
+                    sets.append(([cp(a[:M]) for a in A_full], [cp(b) for b in B_full],
+                                 torch.empty((M, N), dtype=torch.bfloat16, device=dev),
+                                 torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
+            for path in paths:
+                ws.set_debug({"default": 0, "oneshot": are.DEBUG_AR_ONESHOT, "lamport": are.DEBUG_AR_LAMPORT}[path])
+                kernels = []
+                if op == "allreduce_rmsnorm":
+                    def mk(st):
+                        return lambda: are.allreduce_rmsnorm(st[0], st[1], gamma_d, EPS, st[2], ws)
+                    calls = [mk(sets[i % n_sets]) for i in range(n_calls)]
+                    calls[0]()
+                    kernels.append(ws.last_launch())
+                elif op == "gemm_ar":
+                    def mk(st):
+                        return lambda: are.gemm_ar(st[0], st[1], st[2], ws)
+                    calls = [mk(sets[i % n_sets]) for i in range(n_calls)]
+                    calls[0]()
+                    kernels.append(ws.last_launch())
+                elif op == "gemm_rs":
+                    def mk(st):
+                        return lambda: are.gemm_rs(st[0], st[1], st[2], ws)
+                    calls = [mk(sets[i % n_sets]) for i in range(n_calls)]
+                    calls[0]()
+                    kernels.append(ws.last_launch())
+                else:
+                    def mk(st):
+                        def c():
+                            are.gemm_rs(st[0], st[1], st[2], ws)
+                            are.allreduce_rmsnorm([st[2]], None, gamma_d, EPS, st[3], ws)
+                        return c
+                    calls = [mk(sets[i % n_sets]) for i in range(n_calls)]
+                    st0 = sets[0]
+                    are.gemm_rs(st0[0], st0[1], st0[2], ws)
+                    kernels.append(ws.last_launch())
+                    are.allreduce_rmsnorm([st0[2]], None, gamma_d, EPS, st0[3], ws)
+                    kernels.append(ws.last_launch())
+                t0 = time.time()
+                us = time_calls(calls, dev)
+                t1 = time.time()
+                ws.set_debug(0)
+                stw = ws.device_status()
+                if stw["code"] != 0:
+                    raise RuntimeError(f"device status after {name} M={M} {path}: {stw}")
+                med, best = statistics.median(us), min(us)
+                d = {"workload": name, "op": op, "R": R, "M": M, "N": N, "path": path,
+                     "kernels": [f"{k['kernel']} grid={k['grid']}x{k['block']}"
+                                 + (f" rank_block={k['rank_block']}" if k["kernel"] == "gemm_pair_kernel" else "")
+                                 for k in kernels],
+                     "us_median": med, "us_best": best, "calls_per_replay": n_calls, "input_sets": n_sets,
+                     "streamed_per_replay_mb": round(n_calls * byts / 1e6, 1)}
+                if K:
+                    d["K"] = K
+                if flops:
+                    d["tflops"] = flops / (med * 1e-6) / 1e12
+                d["gbs_algorithmic"] = byts / (med * 1e-6) / 1e9
+                for regime in ("burst", "sustained"):
+                    d[f"frac_of_roofline_{regime}"] = roofline_seconds_of(flops, byts, peaks, regime) / (med * 1e-6)
+                d["bound"] = "tensor" if flops / (peaks["bf16_tflops"] * 1e12) > byts / (peaks["hbm_gbs"] * 1e9) \
+                    else "hbm"
+                sampler_windows.append((d, (t0, t1)))
+                results.append(d)
+            del sets
+            torch.cuda.empty_cache()
+    return results
 
 
 # --------------------------------------------------------------------------- GPU arm
@@ -352,6 +602,7 @@ def run_gpu(args):
     torch.cuda.synchronize(dev)
     sampler.start()
     time.sleep(0.3)
+    windows = {}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     w0 = time.time()
@@ -360,8 +611,7 @@ def run_gpu(args):
         step(events[i])
     t_end.record(stream)
     torch.cuda.synchronize(dev)
-    sampler.mark(w0, time.time())
-    clocks = sampler.stop()
+    windows["step"] = (w0, time.time())
     if dist is not None:
         dist.barrier()
     st = ws.device_status()
@@ -386,8 +636,9 @@ def run_gpu(args):
             are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
         o0 = torch.cuda.Event(enable_timing=True)
         o1 = torch.cuda.Event(enable_timing=True)
+        n_alone = max(args.steps, 20)
         o0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(n_alone):
             are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
         o1.record(stream)
         torch.cuda.synchronize(dev)
@@ -395,36 +646,59 @@ def run_gpu(args):
         st = ws.device_status()
         if st["code"] != 0:
             raise RuntimeError(f"device status after AR+RMSNorm alone ({flags}): {st}")
-        return max_over_ranks(dist, o0.elapsed_time(o1) / args.steps, dev)
+        return max_over_ranks(dist, o0.elapsed_time(o1) / n_alone, dev)
 
     lamport_alone_ms = alone(0)
     oneshot_ms = alone(are.DEBUG_AR_ONESHOT)
 
-    roof = {p: roofline_seconds(p, peaks) for p in WORKLOAD}
+    # every workload at every size, one by one (after the step; outside its timed region)
+    cfg_windows = []
+    configs = None
+    if not args.no_configs:
+        configs = run_configs(ws, dev, {"gemm_rs": (A_rs, B_rs), "gemm_ar": (A_ar, B_ar),
+                                              "allreduce_rmsnorm": (P_n, res_n, gamma_n)}, peaks, cfg_windows)
+    sampler.stop()
+    clocks = sampler.summary(windows["step"])
+    regime, regime_why = peak_regime(clocks)
+    for d, win in cfg_windows:
+        c = sampler.summary(win)
+        d["clock_mhz_median"] = c.get("sm_mhz")
+        d["power_cap"] = "sw_power_cap" in (c.get("reasons") or [])
+
+    roof = {p: roofline_seconds(p, peaks, regime) for p in WORKLOAD}
     value = world * 100.0 * sum(roof.values()) / (ms_step * 1e-3)
     parts = {}
     for p in WORKLOAD:
         flops, byts = work(p)
         d = {"ms": per_ms[p], "roofline_ms": roof[p] * 1e3, "frac_of_roofline": roof[p] / (per_ms[p] * 1e-3)}
+        for reg in ("burst", "sustained"):
+            d[f"frac_of_roofline_{reg}"] = roofline_seconds(p, peaks, reg) / (per_ms[p] * 1e-3)
         if flops:
             d["tflops"] = flops / (per_ms[p] * 1e-3) / 1e12
         d["gbs_algorithmic"] = byts / (per_ms[p] * 1e-3) / 1e9
         parts[p] = d
-    peak_t = peaks["bf16_tflops_sustained"]
+    peak_t = bf16_peak(peaks, regime)
     flops_rs, _ = work("gemm_rs")
     ach_rs = flops_rs / (per_ms["gemm_rs"] * 1e-3) / 1e12
     roofline = {"kernel": "gemm_pair_kernel<RS> (gemm_rs)", "bound": "tensor", "achieved": ach_rs,
-                "peak": peak_t, "unit": "TFLOP/s", "frac": ach_rs / peak_t, "traffic": NCU_TRAFFIC["gemm_rs"],
-                "peak_source": f"{source} bf16 sustained", "note": f"of {source}"}
+                "peak": peak_t, "unit": "TFLOP/s", "frac": ach_rs / peak_t, "traffic": ncu_traffic("gemm_rs"),
+                "peak_source": f"{source} bf16 {regime}", "peak_regime_reason": regime_why,
+                "frac_burst": ach_rs / peaks["bf16_tflops"], "frac_sustained": ach_rs / peaks["bf16_tflops_sustained"],
+                "ms_x_mhz": per_ms["gemm_rs"] * (clocks.get("sm_mhz") or 0.0), "note": f"of {source}"}
     _, bytes_n = work("allreduce_rmsnorm")
     ach_n = bytes_n / (per_ms["allreduce_rmsnorm"] * 1e-3) / 1e9
     roofline_ar = {"kernel": "ar_rmsnorm_kernel<4> (allreduce_rmsnorm)", "bound": "hbm", "achieved": ach_n,
                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach_n / peaks["hbm_gbs"],
-                   "traffic": NCU_TRAFFIC["allreduce_rmsnorm"], "peak_source": f"{source} HBM copy",
+                   "traffic": ncu_traffic("allreduce_rmsnorm"), "peak_source": f"{source} HBM copy",
                    "note": f"of {source}; in the step"}
     ach_alone = bytes_n / (lamport_alone_ms * 1e-3) / 1e9
     roofline_ar["alone"] = {"ms": lamport_alone_ms, "achieved": ach_alone, "frac": ach_alone / peaks["hbm_gbs"],
                             "note": "the same kernel, calls back to back outside the step (inputs larger than L2)"}
+    flops_ar, _ = work("gemm_ar")
+    ach_ga = flops_ar / (per_ms["gemm_ar"] * 1e-3) / 1e12
+    roofline_gemm_ar = {"kernel": "gemm_pair_kernel<AR> (gemm_ar)", "bound": "tensor", "achieved": ach_ga,
+                        "peak": peak_t, "unit": "TFLOP/s", "frac": ach_ga / peak_t, "traffic": ncu_traffic("gemm_ar"),
+                        "peak_source": f"{source} bf16 {regime}"}
 
     # ---- end to end: pinned host inputs -> device, the three calls, results -> host
     e2e_steps = max(1, min(args.steps, 5))
@@ -514,13 +788,17 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu_s, threads, sample = oracle_sample_time()
-        cpu = {"value": 100.0 * sum(roof.values()) / cpu_s, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": sample, "ms_per_step_extrapolated": cpu_s * 1e3}
+        # the oracle on the host cores, on one bounded sample of the step: the value is
+        # its throughput on that sample as a fraction of the sampled work's roofline
+        r = oracle_sample_step()
+        cpu = {"value": 100.0 * sample_roofline_seconds(r["fraction"], peaks, regime) / r["seconds"], "unit": UNIT,
+               "cores": r["threads"], "kind": "oracle", "sample": r["sample"], "ms_sample_measured": r["seconds"] * 1e3,
+               "ms_per_step_full_extrapolated": r["full_step_seconds_extrapolated"] * 1e3}
         # the same oracle on one thread, on a smaller row sample
-        cpu1_s, _, sample1 = oracle_sample_time(nthreads=1, gemm_rows=8)
-        cpu["single_thread"] = {"value": 100.0 * sum(roof.values()) / cpu1_s, "cores": 1, "sample": sample1,
-                                "ms_per_step_extrapolated": cpu1_s * 1e3}
+        r1 = oracle_sample_step(nthreads=1, gemm_rows=8)
+        cpu["single_thread"] = {"value": 100.0 * sample_roofline_seconds(r1["fraction"], peaks, regime) / r1["seconds"],
+                                "cores": 1, "sample": r1["sample"], "ms_sample_measured": r1["seconds"] * 1e3,
+                                "ms_per_step_full_extrapolated": r1["full_step_seconds_extrapolated"] * 1e3}
 
     if rank == 0:
         line = {
@@ -530,7 +808,9 @@ def run_gpu(args):
             "config": config_block(),
             "parts": parts,
             "roofline": roofline,
+            "roofline_gemm_ar": roofline_gemm_ar,
             "roofline_allreduce_rmsnorm": roofline_ar,
+            "configs": configs,
             "allreduce_rmsnorm_oneshot": {
                 "kernel": "ar_oneshot_kernel<4> (same workload, path forced; outside the step)",
                 "ms": oneshot_ms, "gbs_algorithmic": work("allreduce_rmsnorm")[1] / (oneshot_ms * 1e-3) / 1e9,
@@ -542,7 +822,7 @@ def run_gpu(args):
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
                     "overlap": "host->device copies, the calls and device->host copies on three streams"},
             "gpu_launches": 3 * args.steps,
-            "peaks": {"source": source, **peaks},
+            "peaks": {"source": source, "regime": regime, **peaks},
         }
         print(json.dumps(line), flush=True)
     ws.close()
@@ -561,6 +841,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload timings (profiling runs)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 10 if args.impl == "reference" else 300

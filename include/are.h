@@ -83,7 +83,8 @@ typedef enum are_status {
     ARE_ETIMEOUT = 4, /* a bounded device wait expired (reported by are_get_device_status) */
     ARE_EBUSY = 5,    /* the workspace is in use by another host thread */
     ARE_ENODEV = 6,   /* the current device is not an sm_103 GPU */
-    ARE_ECAPACITY = 7 /* the call exceeds the capacities the workspace was created with */
+    ARE_ECAPACITY = 7, /* the call exceeds the capacities the workspace (or fixed scratch) was created with */
+    ARE_ECAPTURE = 8   /* a one-time set-up that cannot run inside a stream capture was needed */
 } are_status;
 
 typedef enum are_op {
@@ -154,6 +155,26 @@ enum {
                               phase B span, [8] blocks counted */
 };
 
+/* Which kernel a call launched, see are_debug_last_launch(). */
+typedef enum are_kernel {
+    ARE_KERNEL_NONE = 0,          /* nothing launched (an empty problem) */
+    ARE_KERNEL_MEMSET = 1,        /* K == 0: the outputs were zero-filled with memsets */
+    ARE_KERNEL_GEMM_ONE_CTA = 2,  /* GEMM + reduce, one CTA per 128x256 tile */
+    ARE_KERNEL_GEMM_PAIR = 3,     /* GEMM + reduce, CTA pairs (cta_group::2) per 256x256 block */
+    ARE_KERNEL_AR_LAMPORT = 4,    /* AR+RMSNorm, two phases meeting through -0.0-armed staging words */
+    ARE_KERNEL_AR_ONESHOT = 5     /* AR+RMSNorm, one-shot (no staging) */
+} are_kernel;
+
+typedef struct are_launch_info {
+    int32_t kernel;       /* are_kernel */
+    int32_t grid;         /* CTAs launched */
+    int32_t block;        /* threads per CTA */
+    int32_t cluster;      /* CTAs per cluster (1 or 2) */
+    int32_t rank_block;   /* GEMM pair kernel: tile pairs per rank block, 0 = a pair's R units consecutive */
+    int32_t variant;      /* AR kernels: 8-element packs per thread of a row (template variant) */
+    int32_t reserved[2];
+} are_launch_info;
+
 typedef struct are_ws are_ws;
 
 /* Library version, (major << 16) | minor. */
@@ -163,22 +184,43 @@ ARE_API int are_version(void);
 ARE_API const char* are_status_string(are_status s);
 
 /* The predicate every call applies before launching; ARE_OK if supported.
+ * ROCm/mori PR #662 "Fuse DSV4-Pro wo_b's GEMM with its all-reduce over cco
+ * SDMA", review threads: a capability query and the execution path must share
+ * one predicate, so that a shape the query accepts never fails later at
+ * launch, and a shape it rejects is never run.  Every operation below calls
+ * this same function before it validates pointers or launches anything.
  *  GEMM_RS: 1 <= R <= 8; M, N >= 0; K >= 0; K % 8 == 0 and N % 8 == 0 (16-byte
  *           rows for TMA); M % R == 0 and (M / R) % 8 == 0 (owner segments
  *           start on 8-row boundaries).
  *  GEMM_AR: 1 <= R <= 8; K % 8 == 0; N % 8 == 0.
  *  ALLREDUCE_RMSNORM: 1 <= R <= 8; N % 8 == 0 (16-byte packs); N <= 32768.
- * K is ignored for ALLREDUCE_RMSNORM. */
+ * K is ignored for ALLREDUCE_RMSNORM.  Pure host function: no device needed. */
 ARE_API are_status are_supports(int op, int R, int64_t M, int64_t N, int64_t K);
 
 /* Create a workspace on the current CUDA device: tile masks, the per-rank
  * partial buffer, the Lamport staging buffer (filled with the sentinel, on a
- * private stream, synchronously) and the device status word.  On failure
- * everything acquired so far is released and the first error is returned
- * (*ws is then NULL).  Must not be called during stream capture. */
+ * private stream, synchronously) and the device status word.
+ * ROCm/mori PR #662, review threads: every capacity is validated before the
+ * first allocation; buffer offsets are sized from the capacities, never from
+ * a call's M, so the layout does not move between calls; a set-up that fails
+ * part-way releases everything it acquired and returns the first (original)
+ * error, not the error of the clean-up.  ROCm/aiter PR #4977, bring-up
+ * commits: the staging region is private to this library and is armed here,
+ * outside any stream capture, on a stream of its own (an arming captured into
+ * a graph would re-arm on every replay, under the kernel's feet).
+ *  caps : R_max 1..8, M_max >= 1, N_max >= 8 and N_max % 8 == 0, K_max >= 0.
+ *  ws   : receives the handle; *ws is NULL on any failure.
+ * Returns ARE_EINVAL for bad capacities, ARE_ENODEV if the current device is
+ * not sm_103, ARE_ENOMEM / ARE_ECUDA if an allocation or the arming fails.
+ * Must not be called during stream capture. */
 ARE_API are_status are_workspace_create(are_ws** ws, const are_caps* caps);
 
-/* Release a workspace (synchronises the device first).  NULL is accepted. */
+/* Release a workspace: synchronise the device (so no launched kernel still
+ * uses it), then free every buffer of it.  NULL is accepted.  The caller's
+ * tensors are not touched.  ROCm/mori PR #662, review threads: an op that
+ * owns device buffers releases them through an explicit close, never only
+ * through a destructor at interpreter exit.  Returns the synchronisation's
+ * error, if any (the buffers are freed either way). */
 ARE_API are_status are_workspace_destroy(are_ws* ws);
 
 /* Clear the device status word, zero every tile mask and re-arm every staging
@@ -202,6 +244,11 @@ ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t byte
 /* Synchronise the device, then copy the workspace's device status word.
  * Returns ARE_ETIMEOUT if a device wait expired, else ARE_OK. */
 ARE_API are_status are_get_device_status(are_ws* ws, are_dev_status* out);
+
+/* Host-side record of the last operation called with this workspace: which
+ * kernel it launched and with which launch shape.  Reads no device memory and
+ * does not synchronise.  Zeroed (ARE_KERNEL_NONE) before any call. */
+ARE_API are_status are_debug_last_launch(are_ws* ws, are_launch_info* out);
 
 /* Synchronise the device and copy `bytes` of a bookkeeping buffer (ARE_SNAP_*)
  * to host memory `host_dst`. */
@@ -317,19 +364,34 @@ ARE_API are_status are_allreduce_rmsnorm_quant(const are_bf16* const partials[],
  *           returns ARE_ECAPACITY and launches nothing.
  *  Set-up:  the first call on a device looks up the array's device address
  *           (once per device, with that device current); make that first
- *           call before any stream capture.
+ *           call before any stream capture.  A first call made on a stream
+ *           that is capturing returns ARE_ECAPTURE and enqueues nothing.
  *  Sharing: every call uses the same array and it keeps the last call's
  *           contents.  Each call therefore first clears the status word and
  *           re-arms the staging words it uses with the -0.0 sentinel, on
  *           `stream`, then runs the kernel.  Calls whose kernels can overlap
  *           on the GPU (other streams, other host threads) race on the array
- *           and give undefined results.  A device-side wait that expires is
- *           not reported by this entry point; the output is then undefined.
+ *           and give undefined results.  A device-side wait that expires
+ *           (bounded at 200 ms) is recorded in the array's status word; read
+ *           it with are_noalloc_device_status().
  *  Never calls cudaMalloc, cudaFree or any allocating library routine.
  */
 ARE_API are_status are_allreduce_rmsnorm_noalloc(const are_bf16* const partials[], const are_bf16* residual,
                                                  const float* gamma, float eps, are_bf16* out, int R, int64_t M,
                                                  int64_t N, void* stream);
+
+/*
+ * Device status word of the allocation-free entry point on the current device.
+ * The pages have no counterpart to it: it exists because callers of
+ * are_allreduce_rmsnorm_noalloc have no workspace to ask.  It synchronises the
+ * device, then copies the 16-byte status word at the start of the fixed array
+ * to `out` with cudaMemcpy (no allocation).  Every call of the entry point
+ * clears that word first, so it describes the last call only.  Returns
+ * ARE_ETIMEOUT if a device wait of that call expired (its output is then
+ * undefined), ARE_OK otherwise, ARE_ENODEV / ARE_ECUDA if the current device
+ * cannot be set up, ARE_EINVAL for a NULL `out`.
+ */
+ARE_API are_status are_noalloc_device_status(are_dev_status* out);
 
 #ifdef __cplusplus
 }

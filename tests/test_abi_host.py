@@ -28,7 +28,7 @@ def test_header_declarations_are_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(8):
+    for s in range(9):
         assert lib.are_status_string(s).decode().startswith("ARE_")
 
 
