@@ -71,6 +71,8 @@ def _load(plant: int = 0):
         lib.oracle_tile_pieces.argtypes = [i64, i64, i64, i32, vp, vp, vp]
         lib.oracle_expected_masks.restype = i64
         lib.oracle_expected_masks.argtypes = [i32, i64, i64, i64, i64, vp, i64]
+        lib.oracle_chunk_pieces.restype = None
+        lib.oracle_chunk_pieces.argtypes = [i32, i64, i64, i64, i64, i32, vp]
         lib.oracle_ar_stage.restype = i64
         lib.oracle_ar_stage.argtypes = [vp, i32, i64, i64, vp, i32]
         lib.oracle_rmsnorm_rows.argtypes = [vp, vp, vp, ctypes.c_float, i64, i64, vp, vp, i32]
@@ -166,6 +168,14 @@ class Oracle:
         words = np.zeros(nwords, dtype=np.uint32)
         T = self.lib.oracle_expected_masks(R, M, N, BM, BN, words.ctypes.data, nwords)
         return words, int(T)
+
+    def chunk_pieces(self, R: int, M: int, N: int, C: int,
+                     BM: int = MASK_TILE_M, BN: int = MASK_TILE_N) -> np.ndarray:
+        """[R, C] int64: pieces (one tile's rows stored into one owner segment)
+        that complete chunk c of segment s in one call; 0 for unused chunks."""
+        out = np.zeros(R * C, dtype=np.int64)
+        self.lib.oracle_chunk_pieces(R, M, N, BM, BN, C, out.ctypes.data)
+        return out.reshape(R, C)
 
     def segments(self, Y: np.ndarray, R: int):
         """Split a full [M, N] result into the R owner segments."""

@@ -284,6 +284,39 @@ int64_t oracle_expected_masks(int R, int64_t M, int64_t N, int64_t BM, int64_t B
     return T;
 }
 
+/*
+ * Chunked owner-segment completion ([MORI], the fused GEMM -> scatter
+ * follow-ups: per-(destination, chunk) completion counters; the chunk count
+ * "halved until it divides the M-tiles per destination").  Reading for row
+ * owners: destination s is owner segment s = rows [s*S, (s+1)*S); its M-tiles
+ * are the n_s output tile rows of height BM that intersect it (a tile that
+ * straddles two segments is an M-tile of both).  The requested count C is
+ * halved (integer halving) until it divides n_s, giving C_s chunks; chunk c
+ * of segment s is its tile rows [c*n_s/C_s, (c+1)*n_s/C_s) in increasing
+ * order.  One piece is one output tile's rows stored into one segment, so a
+ * chunk completes after (n_s/C_s) * ceil(N/BN) pieces.  Fills pieces[s*C + c]
+ * with that count for c < C_s and 0 for the chunks a segment does not use.
+ */
+void oracle_chunk_pieces(int R, int64_t M, int64_t N, int64_t BM, int64_t BN, int C, int64_t *pieces) {
+    int64_t S = M / R;
+    int64_t tiles_n = (N + BN - 1) / BN;
+    for (int s = 0; s < R; ++s) {
+        for (int c = 0; c < C; ++c) pieces[(int64_t)s * C + c] = 0;
+        if (S == 0 || tiles_n == 0) continue;
+        int64_t t_lo = ((int64_t)s * S) / BM;
+        int64_t t_hi = ((int64_t)(s + 1) * S - 1) / BM;
+        int64_t n_s = t_hi - t_lo + 1;
+        int64_t cs = C;
+#if ORACLE_PLANT == 7 /* planted: halves only until the count is at most the M-tiles */
+        while (cs > n_s) cs /= 2;
+#else
+        while (cs > 1 && n_s % cs != 0) cs /= 2;
+#endif
+        if (cs < 1) cs = 1;
+        for (int64_t c = 0; c < cs; ++c) pieces[(int64_t)s * C + c] = (n_s / cs) * tiles_n;
+    }
+}
+
 /* ------------------------------------------------------------------------ */
 /* All-reduce + residual + RMSNorm  [LAMP]                                    */
 /* ------------------------------------------------------------------------ */

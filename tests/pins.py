@@ -227,6 +227,39 @@ def pin_masks_golden(o):
         assert np.all(words[:T] == full) and np.all(words[T:] == 0), "mask words wrong"
 
 
+def pin_chunk_pieces_golden(o):
+    for lhs, rhs in _read_golden("chunks.txt"):
+        R, M, N, C = map(int, lhs)
+        want = np.array([[int(v) for v in seg.split(",")] for seg in rhs], dtype=np.int64)
+        got = o.chunk_pieces(R, M, N, C)
+        assert got.shape == want.shape and np.array_equal(got, want), \
+            f"chunk_pieces(R={R},M={M},N={N},C={C}) =\n{got}\nwant\n{want}"
+
+
+def pin_chunk_pieces_cover_owner_pieces(o):
+    """Over the chunks of a segment the counts add up to the number of owner
+    pieces stored into that segment in one call (from the owner-piece cut,
+    pinned on its own), every used chunk has the same count, and the used
+    chunks are a prefix whose length divides the segment's tile rows."""
+    for (R, M, N, C) in [(3, 264, 320, 2), (8, 4096, 7168, 8), (4, 1024, 4096, 3), (6, 4800, 512, 4),
+                         (8, 8192, 8192, 16), (2, 64, 256, 4), (5, 1000, 1000, 8)]:
+        tiles_n = -(-N // 256)
+        per_seg = np.zeros(R, np.int64)
+        rows_of_seg = [set() for _ in range(R)]
+        for row0 in range(0, M, 128):
+            for (s, b, e) in o.tile_pieces(row0, 128, M, R):
+                per_seg[s] += tiles_n
+                rows_of_seg[s].add(row0 // 128)
+        got = o.chunk_pieces(R, M, N, C)
+        for s in range(R):
+            assert got[s].sum() == per_seg[s], (R, M, N, C, s, got[s], per_seg[s])
+            used = got[s][got[s] > 0]
+            k = len(used)
+            assert k >= 1 and np.all(got[s][:k] > 0) and np.all(got[s][k:] == 0), (R, M, C, got[s])
+            assert np.all(used == used[0]), (R, M, C, got[s])
+            assert len(rows_of_seg[s]) % k == 0 and k <= C, (R, M, C, got[s])
+
+
 # ---------------------------------------------------------------------------
 # Lamport stage: ring-order sum + canonicalisation
 # ---------------------------------------------------------------------------
@@ -390,6 +423,7 @@ ALL_PINS = [
     pin_bf16_rne, pin_partial_vs_fp64, pin_partial_exact_integers, pin_partial_rectangular,
     pin_rs_vs_fp64, pin_rs_identity_ring_order, pin_rs_one_hot, pin_rs_rows_subset, pin_ar_rounds_partials,
     pin_owner_pieces_golden, pin_owner_pieces_partition, pin_masks_golden,
+    pin_chunk_pieces_golden, pin_chunk_pieces_cover_owner_pieces,
     pin_sentinels_golden, pin_stage_r1_and_order,
     pin_rmsnorm_vs_torch, pin_rmsnorm_closed_forms, pin_bf16_rne_array, pin_residual_out,
     pin_e4m3_vs_torch, pin_quant_rows,

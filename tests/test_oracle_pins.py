@@ -12,8 +12,9 @@ def test_pin(pin, oracle):
 
 # Each planted mistake (see ORACLE_PLANT in oracle.c) must be caught by at
 # least one pin: a transposed operand, a dropped rank, a wrong sign, an
-# off-by-one owner, a skipped canonicalisation, eps outside the square root.
-@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6])
+# off-by-one owner, a skipped canonicalisation, eps outside the square root,
+# a chunk count halved by the wrong rule.
+@pytest.mark.parametrize("plant", [1, 2, 3, 4, 5, 6, 7])
 def test_pins_catch_planted_mistake(plant):
     o = oracle_mod.Oracle(plant=plant)
     failed = []
