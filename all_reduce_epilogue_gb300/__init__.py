@@ -33,7 +33,9 @@ DEBUG_SINGLE_CTA, DEBUG_WAIT_PROFILE, DEBUG_AR_ONESHOT, DEBUG_AR_LAMPORT, DEBUG_
 # device status codes
 DEV_OK, DEV_MASK_TIMEOUT, DEV_STAGE_TIMEOUT, DEV_PIPE_TIMEOUT = 0, 1, 2, 3
 # snapshot kinds
-SNAP_MASKS, SNAP_STAGING, SNAP_PIECES, SNAP_COUNTERS = 1, 2, 3, 4
+SNAP_MASKS, SNAP_STAGING, SNAP_PIECES, SNAP_COUNTERS, SNAP_CHUNKS = 1, 2, 3, 4, 5
+CHUNK_CAP = 64          # chunk counters per owner segment in the workspace
+CHUNK_Q = 1 << 32       # counter advance per completed chunk
 # kernels (are_kernel), as reported by Workspace.last_launch()
 KERNEL_NAMES = {0: "none", 1: "memset", 2: "gemm_reduce_kernel", 3: "gemm_pair_kernel", 4: "ar_rmsnorm_kernel",
                 5: "ar_oneshot_kernel"}
@@ -44,6 +46,7 @@ TILE_M, TILE_N = 128, 256
 EXPORTS = [
     "are_version", "are_status_string", "are_supports", "are_workspace_create", "are_workspace_destroy",
     "are_workspace_reset", "are_workspace_set_debug", "are_workspace_set_oneshot_max_bytes",
+    "are_workspace_set_gemm_order", "are_workspace_set_chunks", "are_chunk_generation", "are_chunk_wait",
     "are_get_device_status", "are_debug_snapshot", "are_debug_last_launch",
     "are_gemm_rs", "are_gemm_ar", "are_allreduce_rmsnorm", "are_allreduce_add_rmsnorm", "are_allreduce_rmsnorm_quant",
     "are_allreduce_rmsnorm_noalloc", "are_noalloc_device_status",
@@ -73,7 +76,7 @@ class _DevStatus(ctypes.Structure):
 class _LaunchInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("grid", ctypes.c_int32), ("block", ctypes.c_int32),
                 ("cluster", ctypes.c_int32), ("rank_block", ctypes.c_int32), ("variant", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("rank_group", ctypes.c_int32), ("group_m", ctypes.c_int32)]
 
 
 _lib = None
@@ -105,6 +108,14 @@ def load_library(path: str = LIB_PATH):
     lib.are_workspace_set_debug.argtypes = [vp, u32, i64]
     lib.are_workspace_set_oneshot_max_bytes.restype = i32
     lib.are_workspace_set_oneshot_max_bytes.argtypes = [vp, u64]
+    lib.are_workspace_set_gemm_order.restype = i32
+    lib.are_workspace_set_gemm_order.argtypes = [vp, i32, i32, i32]
+    lib.are_workspace_set_chunks.restype = i32
+    lib.are_workspace_set_chunks.argtypes = [vp, i32, i32]
+    lib.are_chunk_generation.restype = i32
+    lib.are_chunk_generation.argtypes = [vp, ctypes.POINTER(u64)]
+    lib.are_chunk_wait.restype = i32
+    lib.are_chunk_wait.argtypes = [vp, i32, i32, u64, u64]
     lib.are_get_device_status.restype = i32
     lib.are_get_device_status.argtypes = [vp, ctypes.POINTER(_DevStatus)]
     lib.are_debug_snapshot.restype = i32
@@ -228,7 +239,39 @@ class Workspace:
         li = _LaunchInfo()
         _check(load_library().are_debug_last_launch(self.handle, ctypes.byref(li)), "are_debug_last_launch")
         return {"kernel": KERNEL_NAMES.get(li.kernel, str(li.kernel)), "grid": li.grid, "block": li.block,
-                "cluster": li.cluster, "rank_block": li.rank_block, "variant": li.variant}
+                "cluster": li.cluster, "rank_block": li.rank_block, "variant": li.variant,
+                "rank_group": li.rank_group, "group_m": li.group_m}
+
+    def set_gemm_order(self, group_m: int = 0, block_pairs: int = 0, rank_group: int = 0):
+        """Order of the CTA-pair GEMM kernel's work units (0 = the library's
+        choice; block_pairs < 0 = a pair's R units consecutive).  Results do
+        not depend on it."""
+        _check(load_library().are_workspace_set_gemm_order(self.handle, group_m, block_pairs, rank_group),
+               "are_workspace_set_gemm_order")
+
+    def set_chunks(self, chunks: int, stripe: int = 0):
+        """GEMM+RS chunked owner-segment completion: `chunks` per segment (0 =
+        off); `stripe` 0 = destination-rotated chunk-major order, > 0 = striped,
+        -1 = the usual order."""
+        _check(load_library().are_workspace_set_chunks(self.handle, chunks, stripe), "are_workspace_set_chunks")
+
+    def chunk_generation(self) -> int:
+        g = ctypes.c_uint64()
+        _check(load_library().are_chunk_generation(self.handle, ctypes.byref(g)), "are_chunk_generation")
+        return g.value
+
+    def chunk_wait(self, segment: int, chunk: int, generation: int, timeout_ns: int = 1_000_000_000) -> bool:
+        """Host-side wait for a chunk to reach `generation`; False on timeout."""
+        rc = load_library().are_chunk_wait(self.handle, segment, chunk, generation, timeout_ns)
+        if rc not in (OK, ETIMEOUT):
+            raise AreError(rc, "are_chunk_wait")
+        return rc == OK
+
+    def chunk_counters(self):
+        """[R_max, CHUNK_CAP] uint64 completion counters (synchronises)."""
+        import numpy as np
+        n = self.caps["R_max"] * CHUNK_CAP * 8
+        return self.snapshot(SNAP_CHUNKS, n).view(np.uint64).reshape(self.caps["R_max"], CHUNK_CAP)
 
     def snapshot(self, kind: int, nbytes: int):
         import numpy as np

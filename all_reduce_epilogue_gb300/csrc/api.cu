@@ -11,6 +11,8 @@
 //    (on a private stream), and the persistent grid is clamped to the
 //    co-resident block count.
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -43,6 +45,16 @@ struct are_ws {
     uint64_t timeout_ns = 0;
     int64_t last_ar_M = 0, last_ar_N = 0;
     int pair_clusters = 0;            // co-resident clusters of the pair kernel on `device`
+    int order_group_m = 0;            // pair-kernel unit order overrides (0 = the library's choice)
+    int order_block = 0;
+    int order_rank_group = 0;
+    // chunked owner-segment completion (GEMM+RS)
+    unsigned long long* d_chunk_ctr = nullptr;  // [R_max][kChunkCap] monotonic counters
+    uint32_t* h_chunk_gen = nullptr;            // [R_max][kChunkCap] completed generations (mapped host memory)
+    uint32_t* d_chunk_gen = nullptr;            // the same memory as the device sees it
+    int chunks = 0;                             // chunks per owner segment, 0 = off
+    int chunk_stripe = 0;                       // destination-rotated order: columns per rotation
+    uint64_t rs_generation = 0;                 // GEMM+RS kernels launched with chunking on
     are_launch_info last{};           // what the last operation launched
 };
 
@@ -81,6 +93,8 @@ void free_ws(are_ws* ws) {
     cudaFree(ws->d_part);
     cudaFree(ws->d_pieces);
     cudaFree(ws->d_staging);
+    cudaFree(ws->d_chunk_ctr);
+    if (ws->h_chunk_gen) cudaFreeHost(ws->h_chunk_gen);
     delete ws;
 }
 
@@ -96,9 +110,15 @@ are_status arm_workspace(are_ws* ws) {
     if (e == cudaSuccess && ws->d_mask) e = cudaMemsetAsync(ws->d_mask, 0, ws->mask_words * 4, s);
     if (e == cudaSuccess && ws->d_pieces) e = cudaMemsetAsync(ws->d_pieces, 0, ws->piece_words * 4, s);
     if (e == cudaSuccess && ws->d_staging) e = launch_fill_u32(ws->d_staging, kSentinelF32, ws->staging_words, s);
+    if (e == cudaSuccess && ws->d_chunk_ctr)
+        e = cudaMemsetAsync(ws->d_chunk_ctr, 0, (size_t)ws->caps.R_max * kChunkCap * 8, s);
     cudaError_t e2 = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = e2;
     cudaStreamDestroy(s);
+    if (e == cudaSuccess && ws->h_chunk_gen) {
+        std::memset(ws->h_chunk_gen, 0, (size_t)ws->caps.R_max * kChunkCap * 4);
+        ws->rs_generation = 0;
+    }
     return from_cuda(e);
 }
 
@@ -208,6 +228,11 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     p->flags = ws->debug_flags;
     p->debug_arg = ws->debug_arg;
     p->timeout_ns = ws->timeout_ns;
+    if (mode == kModeRS && ws->chunks > 0) {
+        p->chunk_ctr = ws->d_chunk_ctr;
+        p->chunk_host = ws->d_chunk_gen;
+        p->chunks = ws->chunks;
+    }
     // CTA pairs (256-row tiles) wherever there are at least two tile rows and
     // the device can co-schedule the clusters; one CTA per tile otherwise.
     const int clusters = ws->pair_clusters;
@@ -227,20 +252,43 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         // are better spread over the waves).
         const int64_t rs_block = 2 * (int64_t)clusters;
         if (mode == kModeRS && (int64_t)p->pairs_m * tiles_n >= 3 * rs_block) p->block_tiles = (int)rs_block;
+        p->rank_group = 1;
+        // caller's order overrides (are_workspace_set_gemm_order); they change the
+        // order of the work units only, never the arithmetic
+        if (ws->order_group_m > 0) p->group_m = (int)std::min<int64_t>(p->pairs_m, ws->order_group_m);
+        if (ws->order_block > 0) {
+            p->block_tiles = ws->order_block;
+            p->rank_group = ws->order_rank_group > 0 ? std::min(ws->order_rank_group, R) : 1;
+        } else if (ws->order_block < 0) {
+            p->block_tiles = 0;
+        }
+        // destination-rotated order (chunked GEMM+RS): needs owner segments of whole pair
+        // rows; chunk c of every segment then runs before chunk c+1 of any
+        if (p->chunks > 0 && ws->chunk_stripe >= 0 && S % 256 == 0) {
+            const int ps = (int)(S / 256);
+            int cs = ws->chunks;
+            while (cs > 1 && ps % cs) cs >>= 1;
+            p->rot_ps = ps;
+            p->rot_cs = cs;
+            p->rot_pc = ps / cs;
+            p->rot_w = ws->chunk_stripe > 0 ? std::min<int>(ws->chunk_stripe, (int)tiles_n) : (int)tiles_n;
+        }
         if (p->block_tiles > 0) {
             const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
             const int64_t blocks = (num_pairs + p->block_tiles - 1) / p->block_tiles;
             p->num_pair_units = (int)(blocks * p->block_tiles * R);
         }
         const int grid = 2 * (int)std::min<int64_t>(p->num_pair_units, clusters);
-        ws->last = are_launch_info{ARE_KERNEL_GEMM_PAIR, grid, gemm_pair_threads(), 2, p->block_tiles, 0, {0, 0}};
+        ws->last = are_launch_info{ARE_KERNEL_GEMM_PAIR, grid, gemm_pair_threads(), 2, p->block_tiles, 0,
+                                   p->block_tiles > 0 ? p->rank_group : R, p->group_m};
         e = launch_gemm_pair(*p, mode, grid, s);
     } else {
         p->group_m = (int)std::min<int64_t>(tiles_m, 8);
         const int grid = (int)std::min<int64_t>(p->num_units, ws->num_sms);
-        ws->last = are_launch_info{ARE_KERNEL_GEMM_ONE_CTA, grid, kGemmThreads, 1, 0, 0, {0, 0}};
+        ws->last = are_launch_info{ARE_KERNEL_GEMM_ONE_CTA, grid, kGemmThreads, 1, 0, 0, R, p->group_m};
         e = launch_gemm_reduce(*p, mode, grid, s);
     }
+    if (e == cudaSuccess && p->chunk_ctr) ++ws->rs_generation;
     delete p;
     return from_cuda(e);
 }
@@ -318,6 +366,12 @@ are_status are_workspace_create(are_ws** out, const are_caps* caps) {
         e = cudaMalloc(&ws->d_mask, ws->mask_words * 4);
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_part, ws->part_bytes);
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_pieces, ws->piece_words * 4);
+        if (e == cudaSuccess) e = cudaMalloc(&ws->d_chunk_ctr, (size_t)caps->R_max * kChunkCap * 8);
+        if (e == cudaSuccess)
+            e = cudaHostAlloc(reinterpret_cast<void**>(&ws->h_chunk_gen), (size_t)caps->R_max * kChunkCap * 4,
+                              cudaHostAllocMapped);
+        if (e == cudaSuccess)
+            e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&ws->d_chunk_gen), ws->h_chunk_gen, 0);
         if (e == cudaSuccess) e = gemm_prepare_kernels();
         if (e == cudaSuccess) ws->pair_clusters = gemm_pair_max_clusters();
     }
@@ -368,6 +422,52 @@ are_status are_workspace_set_debug(are_ws* ws, uint32_t flags, int64_t arg) {
     return ARE_OK;
 }
 
+are_status are_workspace_set_gemm_order(are_ws* ws, int group_m, int block_pairs, int rank_group) {
+    if (!ws || group_m < 0 || rank_group < 0 || rank_group > kMaxRanks) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    ws->order_group_m = group_m;
+    ws->order_block = block_pairs;
+    ws->order_rank_group = rank_group;
+    return ARE_OK;
+}
+
+are_status are_workspace_set_chunks(are_ws* ws, int chunks, int stripe) {
+    if (!ws || chunks < 0 || chunks > kChunkCap || stripe < -1) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    if (chunks > 0 && !ws->d_chunk_ctr) return ARE_ECAPACITY;
+    ws->chunks = chunks;
+    ws->chunk_stripe = stripe;
+    return ARE_OK;
+}
+
+are_status are_chunk_generation(are_ws* ws, uint64_t* generation) {
+    if (!ws || !generation) return ARE_EINVAL;
+    TryLock lk(ws->mu);
+    if (!lk.ok) return ARE_EBUSY;
+    *generation = ws->rs_generation;
+    return ARE_OK;
+}
+
+are_status are_chunk_wait(are_ws* ws, int segment, int chunk, uint64_t generation, uint64_t timeout_ns) {
+    if (!ws || !ws->h_chunk_gen || segment < 0 || segment >= ws->caps.R_max || chunk < 0 || chunk >= kChunkCap)
+        return ARE_EINVAL;
+    // the mapped word holds the chunk's generation modulo 2^32; compare in that ring
+    const volatile uint32_t* w = ws->h_chunk_gen + (size_t)segment * kChunkCap + chunk;
+    const uint32_t want = (uint32_t)generation;
+    const auto t0 = std::chrono::steady_clock::now();
+    for (;;) {
+        if ((int32_t)(*w - want) >= 0) {
+            std::atomic_thread_fence(std::memory_order_acquire);
+            return ARE_OK;
+        }
+        const auto dt = std::chrono::steady_clock::now() - t0;
+        if ((uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(dt).count() > timeout_ns)
+            return ARE_ETIMEOUT;
+    }
+}
+
 are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t bytes) {
     if (!ws) return ARE_EINVAL;
     TryLock lk(ws->mu);
@@ -407,6 +507,8 @@ are_status are_debug_snapshot(are_ws* ws, int kind, void* host_dst, size_t bytes
         case ARE_SNAP_STAGING: src = ws->d_staging; avail = ws->staging_words * 4; break;
         case ARE_SNAP_PIECES: src = ws->d_pieces; avail = ws->piece_words * 4; break;
         case ARE_SNAP_COUNTERS: src = ws->d_counters; avail = kCounterWords * 8; break;
+        case ARE_SNAP_CHUNKS: src = ws->d_chunk_ctr; avail = ws->d_chunk_ctr ? (size_t)ws->caps.R_max * kChunkCap * 8 : 0;
+            break;
         default: return ARE_EINVAL;
     }
     if (!src || bytes > avail) return ARE_EINVAL;
@@ -489,10 +591,10 @@ are_status allreduce_rmsnorm_call(const are_bf16* const partials[], const are_bf
                          ((ws->debug_flags & ARE_DEBUG_AR_ONESHOT) || (uint64_t)M * (uint64_t)N * 2 <= ws->oneshot_max_bytes);
     if (oneshot) {
         const int os_grid = (int)std::min<int64_t>(M, ws->num_sms);
-        ws->last = are_launch_info{ARE_KERNEL_AR_ONESHOT, os_grid, ar_oneshot_threads(), 1, 0, ppt, {0, 0}};
+        ws->last = are_launch_info{ARE_KERNEL_AR_ONESHOT, os_grid, ar_oneshot_threads(), 1, 0, ppt, 0, 0};
         return from_cuda(launch_ar_oneshot(p, ppt, os_grid, s));
     }
-    ws->last = are_launch_info{ARE_KERNEL_AR_LAMPORT, grid, kArThreads, 1, 0, ppt, {0, 0}};
+    ws->last = are_launch_info{ARE_KERNEL_AR_LAMPORT, grid, kArThreads, 1, 0, ppt, 0, 0};
     return from_cuda(launch_ar_rmsnorm(p, ppt, grid, s));
 }
 

@@ -88,6 +88,8 @@ constexpr int kSubBytes = 16384;      // one 128-row x 128-byte sub-tile
 constexpr int kTilePartBytes = 131072;  // fp32 128x256 partial (bf16 uses the first half)
 constexpr int kGemmThreads = 256;
 constexpr int kPieceWords = 64;       // debug piece log words per tile
+constexpr int kChunkCap = 64;         // completion counters per owner segment (largest chunk count)
+constexpr unsigned long long kChunkQ = 1ull << 32;  // counter advance per completed chunk
 
 enum GemmMode : int { kModeRS = 0, kModeAR = 1 };
 
@@ -109,7 +111,17 @@ struct GemmParams {
     int tiles_m, tiles_n, num_tiles, num_units, num_kb;
     int pairs_m, num_pair_units;  // CTA-pair kernel: 256-row tile pairs, R units per pair
     int block_tiles;     // CTA-pair kernel: tile pairs per rank block (0 = ranks innermost)
+    int rank_group;      // CTA-pair kernel: ranks run together inside a block (1 = rank by rank)
     int group_m;         // tile raster: rows of tiles (pairs) per group
+    // chunked owner-segment completion (GEMM+RS; chunk_ctr == nullptr: off)
+    unsigned long long* chunk_ctr;  // [R][kChunkCap] monotonic completion counters
+    uint32_t* chunk_host;           // [R][kChunkCap] completed generation, host-mapped (may be null)
+    int chunks;          // requested chunks per owner segment
+    // destination-rotated order of the pair kernel (rot_pc == 0: raster order)
+    int rot_pc;          // pair rows per order chunk
+    int rot_cs;          // order chunks per owner segment
+    int rot_ps;          // pair rows per owner segment
+    int rot_w;           // tile columns per destination rotation (stripe)
     uint32_t flags;
     int64_t debug_arg;
     uint64_t timeout_ns;

@@ -166,6 +166,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Chunked owner-segment completion (ROCm/mori PR #662, the fused GEMM ->
+// scatter follow-ups: per-(destination, chunk) completion counters, monotonic,
+// with a modulo election).  The destinations are the owner segments: chunk c
+// of segment s is a band of the n_s tile rows that intersect s, the requested
+// chunk count halved until it divides n_s.  A reducer tile stores one piece
+// into every segment its rows meet; once those stores have completed it adds
+// 1 to each piece's (segment, chunk) counter with release.  The counters are
+// never reset: every call starts at a multiple of kChunkQ, so the low 32 bits
+// count this call's pieces, and the one add that sees `pieces - 1` there is
+// the chunk's last (the modulo election).  The elected thread advances the
+// counter to the next multiple of kChunkQ, so the next call starts at zero
+// pieces whatever its shape, and publishes the chunk's generation (counter /
+// kChunkQ) to the host-mapped word a host-side waiter polls.
+__device__ __noinline__ void chunk_bump_tile(const GemmParams& p, int tm) {
+    const int row0 = tm * kBM;
+    const int row_end = min(row0 + kBM, p.M);
+    for (int r0 = row0; r0 < row_end;) {
+        const int s = r0 / p.S;
+        const int e = min((s + 1) * p.S, row_end);
+        const int t_lo = (int)(((long long)s * p.S) / kBM);
+        const int t_hi = (int)(((long long)(s + 1) * p.S - 1) / kBM);
+        const int n_s = t_hi - t_lo + 1;
+        int cs = p.chunks;
+        while (cs > 1 && n_s % cs) cs >>= 1;
+        const int per = n_s / cs;
+        const int idx = s * kChunkCap + (tm - t_lo) / per;
+        const unsigned long long pieces = (unsigned long long)per * (unsigned long long)p.tiles_n;
+        const unsigned long long old = ptx::atom_add_release_gpu_u64(&p.chunk_ctr[idx], 1ull);
+        if ((old & (kChunkQ - 1)) + 1 == pieces) {
+            if (!(p.flags & ARE_DEBUG_NO_REARM)) ptx::atom_add_release_gpu_u64(&p.chunk_ctr[idx], kChunkQ - pieces);
+            if (p.chunk_host) ptx::st_release_sys(&p.chunk_host[idx], (uint32_t)((old >> 32) + 1));
+        }
+        r0 = e;
+    }
+}
+
 // One 128-byte row of a 128B-swizzled 128-row sub-tile: 16-byte chunk c of row
 // `row` lives at chunk position c ^ (row & 7).
 __device__ __forceinline__ void write_row_sw128(uint8_t* base, int row, const uint32_t (&w)[32]) {
@@ -372,6 +408,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
         const int row = threadIdx.x - 128;  // tile row == TMEM lane
         const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
         const bool lead = (warp == 4);
+        int prev_tm = -1;  // chunk counting: the last reducer tile whose stores may still be in flight
         int it = 0, ps = 0;
         uint32_t pph = 0;
         bool bad = false;
@@ -534,6 +571,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
                     }
                 }
                 if (bad) break;
+                if (MODE == kModeRS && p.chunk_ctr && lead) {
+                    // count the previous reducer tile's pieces once its stores have completed:
+                    // each issuing lane waits for all but its groups of this tile (chunks lane, lane+2)
+                    if (lane < 2 && prev_tm >= 0) {
+                        int n = 0;
+                        for (int c = lane; c < kBN / 64; c += 2) n += (U.tn * kBN + c * 64 < p.N) ? 1 : 0;
+                        ptx::bulk_wait_upto(n);
+                    }
+                    __syncwarp();
+                    if (lane == 0 && prev_tm >= 0) {
+                        ptx::fence_proxy_async_global();
+                        chunk_bump_tile(p, prev_tm);
+                    }
+                    prev_tm = U.tm;
+                }
                 if (lead && lane == 0) {
                     if (MODE == kModeRS && (p.flags & ARE_DEBUG_LOG_PIECES)) {
                         int32_t* log = p.pieces + (size_t)U.t * kPieceWords;
@@ -556,6 +608,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
         }
         if (bad) *abort_flag = 1u;
         if (lead && lane < 2) ptx::bulk_wait0();
+        if (MODE == kModeRS && p.chunk_ctr && lead) {
+            __syncwarp();
+            if (lane == 0 && prev_tm >= 0 && !bad) {
+                ptx::fence_proxy_async_global();
+                chunk_bump_tile(p, prev_tm);
+            }
+        }
     }
 
     __syncwarp();
@@ -622,20 +681,28 @@ struct PUnit {
 };
 
 // Pair-unit order.  block_tiles == 0: the R units of a tile pair are
-// consecutive (ranks innermost).  block_tiles == B: tile pairs are taken in
-// blocks of B (in raster order) and a block's units run rank by rank: the j-th
-// unit of every pair in the block, then the (j+1)-th, so a wave streams the
-// operands of one or two ranks; the reducer (j = R-1) stays last per pair.
-// Units past the last pair (padding of the last block) are not valid.
+// consecutive (ranks innermost).  block_tiles == B with rank_group == g: tile
+// pairs are taken in blocks of B (in raster order); inside a block the ranks
+// run in groups of g: for the k-th group, every pair of the block runs its
+// units j = k*g .. k*g+g-1 (consecutively) before the next group starts.  g = 1
+// is rank by rank (a wave streams the operands of one or two ranks), g = R is
+// ranks innermost.  The reducer (j = R-1) stays last per pair.  Units past the
+// last pair (padding of the last block) are not valid.
 __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int u, int q) {
     PUnit U;
     int tp, j;
     if (p.block_tiles > 0) {
-        const int per_block = p.block_tiles * p.R;
+        const int B = p.block_tiles;
+        const int g = p.rank_group > 0 ? p.rank_group : 1;
+        const int per_block = B * p.R;
         const int blk = u / per_block;
-        const int rem = u - blk * per_block;
-        j = rem / p.block_tiles;
-        tp = blk * p.block_tiles + (rem - j * p.block_tiles);
+        int rem = u - blk * per_block;
+        const int k = rem / (B * g);           // rank group
+        const int gk = min(g, p.R - k * g);    // ranks in this group
+        rem -= k * B * g;
+        const int pib = rem / gk;              // pair in block
+        j = k * g + (rem - pib * gk);
+        tp = blk * B + pib;
     } else {
         tp = u / p.R;
         j = u - tp * p.R;
@@ -648,13 +715,33 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
         U.valid = false;
         return U;
     }
-    const int per_group = p.group_m * p.tiles_n;
-    const int g = tp / per_group;
-    const int first = g * p.group_m;
-    const int gm = min(p.pairs_m - first, p.group_m);
-    const int in = tp - g * per_group;
-    const int tmp = first + in % gm;
-    U.tn = in / gm;
+    int tmp;
+    if (p.rot_pc > 0) {
+        // destination-rotated, chunk-major order (ROCm/mori PR #662, the follow-ups on
+        // the destination-rotated tile order and its striped variant): chunk c of every
+        // owner segment before chunk c+1 of any; inside a chunk, every segment's band
+        // of rot_w tile columns before the next band of columns
+        const int Pc = p.rot_pc, W = p.rot_w, TN = p.tiles_n;
+        const int per_c = p.R * Pc * TN;
+        const int c = tp / per_c;
+        int rem = tp - c * per_c;
+        const int ngroups = (TN + W - 1) / W;
+        const int gi = min(rem / (p.R * Pc * W), ngroups - 1);
+        rem -= gi * p.R * Pc * W;
+        const int Wg = min(W, TN - gi * W);
+        const int s = rem / (Pc * Wg);
+        rem -= s * Pc * Wg;
+        tmp = s * p.rot_ps + c * Pc + rem % Pc;
+        U.tn = gi * W + rem / Pc;
+    } else {
+        const int per_group = p.group_m * p.tiles_n;
+        const int g = tp / per_group;
+        const int first = g * p.group_m;
+        const int gm = min(p.pairs_m - first, p.group_m);
+        const int in = tp - g * per_group;
+        tmp = first + in % gm;
+        U.tn = in / gm;
+    }
     U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
     int r = U.own + 1 + j;
     while (r >= p.R) r -= p.R;
@@ -1006,6 +1093,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         // ------------------------------------------------------------ reduce (reducer units of this CTA)
         const int row = threadIdx.x - 256;
         const bool lead = (warp == 8);
+        int prev_tm = -1;  // chunk counting: the last reducer tile whose stores may still be in flight
         int ps = 0;
         uint32_t pph = 0;
         bool bad = false;
@@ -1139,11 +1227,28 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 }
                 // re-arm the tile's mask word for the next call
                 if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
+                if (MODE == kModeRS && p.chunk_ctr) {
+                    // count the previous reducer tile's pieces once its stores have completed
+                    // (all but this tile's bulk groups); this tile's are counted after the next
+                    if (prev_tm >= 0) {
+                        const int rem_cols = p.N - U.tn * kBN;
+                        ptx::bulk_wait_upto(min(kBN / 64, (rem_cols + 63) / 64));
+                        ptx::fence_proxy_async_global();
+                        chunk_bump_tile(p, prev_tm);
+                    }
+                    prev_tm = U.tm;
+                }
             }
         }
         if (bad) *abort_flag = 1u;
         if (lead && lane == 0) prof_add(p, 7, w_pfull);
-        if (lead && lane == 0) ptx::bulk_wait0();
+        if (lead && lane == 0) {
+            ptx::bulk_wait0();
+            if (MODE == kModeRS && p.chunk_ctr && prev_tm >= 0 && !bad) {
+                ptx::fence_proxy_async_global();
+                chunk_bump_tile(p, prev_tm);
+            }
+        }
     }
 
     __syncwarp();

@@ -375,13 +375,16 @@ def config_block():
 
 # --------------------------------------------------------------------------- every workload, one by one
 
-# (name, op, R, M list, N, K, seed config, input distribution)
+# (name, op, R, M list, N, K, seed config, input distribution, chunks per owner segment)
 CONFIGS = [
-    ("tiny gemm_rs + rmsnorm", "gemm_rs_rmsnorm", 2, [64], 256, 128, 0, "uniform"),
-    ("gemm_rs R=4", "gemm_rs", 4, [256, 1024, 4096, 8192], 4096, 2048, 1, "normal"),
-    ("gemm_ar R=8", "gemm_ar", 8, [64, 512, 4096], 7168, 2048, 2, "normal"),
-    ("allreduce_rmsnorm R=8", "allreduce_rmsnorm", 8, [1, 16, 128, 1024, 4096], 7168, 0, 3, "normal"),
-    ("large gemm_rs R=8", "gemm_rs", 8, [8192], 8192, 4096, 4, "normal"),
+    ("tiny gemm_rs + rmsnorm", "gemm_rs_rmsnorm", 2, [64], 256, 128, 0, "uniform", 0),
+    ("gemm_rs R=4", "gemm_rs", 4, [256, 1024, 4096, 8192], 4096, 2048, 1, "normal", 0),
+    ("gemm_ar R=8", "gemm_ar", 8, [64, 512, 4096], 7168, 2048, 2, "normal", 0),
+    ("allreduce_rmsnorm R=8", "allreduce_rmsnorm", 8, [1, 16, 128, 1024, 4096], 7168, 0, 3, "normal", 0),
+    ("large gemm_rs R=8", "gemm_rs", 8, [8192], 8192, 4096, 4, "normal", 0),
+    # the same with chunked owner-segment completion (8 chunks per segment) and the
+    # destination-rotated tile order: the cost of the counters and of the order
+    ("large gemm_rs R=8, chunked + rotated", "gemm_rs", 8, [8192], 8192, 4096, 4, "normal", 8),
 ]
 
 
@@ -433,7 +436,7 @@ def run_configs(ws, dev, dev_step, peaks, sampler_windows):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
     results = []
-    for name, op, R, Ms, N, K, cfg, dist_name in CONFIGS:
+    for name, op, R, Ms, N, K, cfg, dist_name, chunks in CONFIGS:
         seed = synth.config_seed(cfg)
         Mmax = max(Ms)
         # inputs at the largest size (row prefixes give the smaller ones)
@@ -479,6 +482,7 @@ def run_configs(ws, dev, dev_step, peaks, sampler_windows):
                                  torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
             for path in paths:
                 ws.set_debug({"default": 0, "oneshot": are.DEBUG_AR_ONESHOT, "lamport": are.DEBUG_AR_LAMPORT}[path])
+                ws.set_chunks(chunks, 0)
                 kernels = []
                 if op == "allreduce_rmsnorm":
                     def mk(st):
@@ -514,11 +518,12 @@ def run_configs(ws, dev, dev_step, peaks, sampler_windows):
                 us = time_calls(calls, dev)
                 t1 = time.time()
                 ws.set_debug(0)
+                ws.set_chunks(0, 0)
                 stw = ws.device_status()
                 if stw["code"] != 0:
                     raise RuntimeError(f"device status after {name} M={M} {path}: {stw}")
                 med, best = statistics.median(us), min(us)
-                d = {"workload": name, "op": op, "R": R, "M": M, "N": N, "path": path,
+                d = {"workload": name, "op": op, "R": R, "M": M, "N": N, "path": path, "chunks": chunks,
                      "kernels": [f"{k['kernel']} grid={k['grid']}x{k['block']}"
                                  + (f" rank_block={k['rank_block']}" if k["kernel"] == "gemm_pair_kernel" else "")
                                  for k in kernels],

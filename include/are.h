@@ -141,6 +141,8 @@ enum {
     ARE_SNAP_MASKS = 1,    /* uint32 per tile (tile index in the kernel's work order) */
     ARE_SNAP_STAGING = 2,  /* fp32 staging words, row-major [M, N] of the last AR+RMSNorm call */
     ARE_SNAP_PIECES = 3,   /* int32 x 64 per tile: tile_m, tile_n, count, then (segment, begin, end) x count */
+    ARE_SNAP_CHUNKS = 5,   /* uint64 x (R_max x 64): chunk completion counters, [segment][chunk], see
+                              are_workspace_set_chunks() */
     ARE_SNAP_COUNTERS = 4  /* uint64 x 16: [0] canonicalised words; with ARE_DEBUG_WAIT_PROFILE, summed over
                               the CTAs, in SM cycles: [1] TMA producer waiting for a free stage, [2] MMA
                               waiting for operands, [3] MMA waiting for a free accumulator, [4] MMA thread
@@ -172,7 +174,8 @@ typedef struct are_launch_info {
     int32_t cluster;      /* CTAs per cluster (1 or 2) */
     int32_t rank_block;   /* GEMM pair kernel: tile pairs per rank block, 0 = a pair's R units consecutive */
     int32_t variant;      /* AR kernels: 8-element packs per thread of a row (template variant) */
-    int32_t reserved[2];
+    int32_t rank_group;   /* GEMM pair kernel: ranks run together inside a rank block (R = ranks innermost) */
+    int32_t group_m;      /* GEMM kernels: tile(-pair) rows per raster group */
 } are_launch_info;
 
 typedef struct are_ws are_ws;
@@ -240,6 +243,70 @@ ARE_API are_status are_workspace_set_debug(are_ws* ws, uint32_t flags, int64_t a
  * single-GPU caller may raise it.  Returns ARE_EINVAL for a NULL workspace,
  * ARE_EBUSY if the workspace is in use by another thread. */
 ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t bytes);
+
+/* Order of the CTA-pair GEMM kernel's work units (tuning; the results do not
+ * depend on it: every tile is still summed in the order r = 0..R-1).  A unit is
+ * one rank's 256x256 partial of one tile pair; the persistent grid takes units
+ * in this order, wave by wave.  The pages leave the order open; DeepGEMM PR #1
+ * (description) notes that a reduce epilogue that backs up stalls the MMA, and
+ * ROCm/mori PR #662 (the destination-rotated order follow-ups) that the tile
+ * order decides when each destination's data completes.
+ *  group_m     : 256-row tile pairs per raster group (tile pairs are taken
+ *                column by column inside a group of group_m pair rows);
+ *                0 = the library's choice (4).
+ *  block_pairs : > 0: tile pairs are taken in blocks of block_pairs, and a
+ *                block's units run in rank groups (below); < 0: the R units of
+ *                a tile pair run consecutively; 0 = the library's choice
+ *                (GEMM+RS with at least three blocks of two waves of pairs:
+ *                blocks of two waves, rank by rank; otherwise consecutive).
+ *  rank_group  : with block_pairs > 0, the number of ranks whose units of a
+ *                block run together (1 = rank by rank, R = a pair's R units
+ *                consecutive); 0 = 1.
+ * Returns ARE_EINVAL for negative group_m / rank_group or rank_group > 8. */
+ARE_API are_status are_workspace_set_gemm_order(are_ws* ws, int group_m, int block_pairs, int rank_group);
+
+/*
+ * Chunked owner-segment completion for GEMM+RS.  ROCm/mori PR #662, the fused
+ * GEMM -> scatter follow-ups: per-(destination, chunk) completion counters,
+ * monotonic and never reset, whose modulo test elects exactly one CTA per
+ * chunk, with the chunk count halved until it divides the destination's
+ * M-tiles; and the destination-rotated, chunk-major tile order (and its
+ * striped variant), so that every destination's first chunk completes early
+ * instead of destination 0's whole slice first.  Here the destinations are the
+ * owner segments: chunk c of segment s is a band of the 128-row output tiles
+ * that intersect s (their count n_s split into C_s = `chunks` halved until it
+ * divides n_s), and it completes once every 128x256 tile of the band has been
+ * reduced and its rows stored into segment s.  The elected reducer publishes
+ * the chunk's generation (how many calls have completed it since the
+ * workspace was created or reset) to host-mapped memory, where
+ * are_chunk_wait() sees it while the kernel is still running.
+ *  chunks : chunks per owner segment, 0 (off, the default) .. 64.
+ *  stripe : the CTA-pair kernel's tile order while chunking is on, where the
+ *           owner segments are whole 256-row tile pairs (M/R % 256 == 0):
+ *           0 = destination-rotated chunk-major (chunk c of every segment, all
+ *           its tile columns, before chunk c+1 of any); > 0 = striped (every
+ *           segment's chunk-c band of `stripe` tile columns before the next
+ *           band); -1 = the library's usual order (counters only).
+ * The results do not depend on either setting.  Returns ARE_EINVAL for values
+ * outside these ranges, ARE_ECAPACITY for a workspace without GEMM buffers.
+ */
+ARE_API are_status are_workspace_set_chunks(are_ws* ws, int chunks, int stripe);
+
+/* The generation that the last GEMM+RS call enqueued on `ws` with chunking on
+ * publishes for each of its chunks when they complete: the number of such
+ * calls that launched a kernel since the workspace was created or reset
+ * (a call with M, N or K equal to 0 launches none and publishes nothing).
+ * Replays of a captured graph are not counted here: each adds one per
+ * captured call.  Host only. */
+ARE_API are_status are_chunk_generation(are_ws* ws, uint64_t* generation);
+
+/* Host-side wait for chunk `chunk` of owner segment `segment` to reach
+ * `generation` (compared modulo 2^32): polls the host-mapped word that the
+ * elected reducer of the chunk writes, so it returns while the GEMM+RS kernel
+ * is still running, as soon as that chunk's rows are in device memory.  No
+ * GPU-side waiter is involved.  Returns ARE_OK, ARE_ETIMEOUT after
+ * `timeout_ns`, ARE_EINVAL for an index outside the workspace. */
+ARE_API are_status are_chunk_wait(are_ws* ws, int segment, int chunk, uint64_t generation, uint64_t timeout_ns);
 
 /* Synchronise the device, then copy the workspace's device status word.
  * Returns ARE_ETIMEOUT if a device wait expired, else ARE_OK. */
