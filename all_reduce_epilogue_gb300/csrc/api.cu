@@ -48,6 +48,7 @@ struct are_ws {
     int order_group_m = 0;            // pair-kernel unit order overrides (0 = the library's choice)
     int order_block = 0;
     int order_rank_group = 0;
+    uint32_t* d_cons = nullptr;       // GEMM+AR row-slice readers done per tile
     // chunked owner-segment completion (GEMM+RS)
     unsigned long long* d_chunk_ctr = nullptr;  // [R_max][kChunkCap] monotonic counters
     uint32_t* h_chunk_gen = nullptr;            // [R_max][kChunkCap] completed generations (mapped host memory)
@@ -94,6 +95,7 @@ void free_ws(are_ws* ws) {
     cudaFree(ws->d_pieces);
     cudaFree(ws->d_staging);
     cudaFree(ws->d_chunk_ctr);
+    cudaFree(ws->d_cons);
     if (ws->h_chunk_gen) cudaFreeHost(ws->h_chunk_gen);
     delete ws;
 }
@@ -112,6 +114,7 @@ are_status arm_workspace(are_ws* ws) {
     if (e == cudaSuccess && ws->d_staging) e = launch_fill_u32(ws->d_staging, kSentinelF32, ws->staging_words, s);
     if (e == cudaSuccess && ws->d_chunk_ctr)
         e = cudaMemsetAsync(ws->d_chunk_ctr, 0, (size_t)ws->caps.R_max * kChunkCap * 8, s);
+    if (e == cudaSuccess && ws->d_cons) e = cudaMemsetAsync(ws->d_cons, 0, ws->mask_words * 4, s);
     cudaError_t e2 = cudaStreamSynchronize(s);
     if (e == cudaSuccess) e = e2;
     cudaStreamDestroy(s);
@@ -243,16 +246,19 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     const bool pair_ok = tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
     if (pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA))) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
-        // GEMM+RS with at least three rank blocks' worth of tile pairs: run the ranks block
-        // by block (two waves of tile pairs per block) so a wave streams one or two ranks'
-        // operands.  A block's reductions all come at its end, and with fewer blocks that
-        // burst is not hidden: R=4, M=4096, N=4096, K=2048 (1.7 blocks) measured 1219 TFLOP/s
-        // with the ranks innermost against 1097 rank-blocked; M=8192 (3.5 blocks) 1323
-        // against 1360.  GEMM+AR keeps the ranks innermost (its reductions write R views and
-        // are better spread over the waves).
+        // GEMM+RS with at least three blocks of two waves of tile pairs: run the ranks block
+        // by block, two ranks at a time, so a wave streams the operands of two ranks.  A
+        // block's reductions all come at its end.  Measured (us per call): the large GEMM+RS
+        // 2662 with blocks of two waves and rank groups of 2, against 2691 with half-wave
+        // blocks rank by rank, 2717 with two-wave blocks rank by rank and 3000 with a pair's
+        // R units consecutive; R=4, M=8192, N=4096, K=2048: 401 against 397 consecutive and
+        // 465 with half-wave blocks.  Below the threshold a block's reduction burst is not
+        // hidden and the ranks stay consecutive (R=4, M=4096: 213 against 220).  GEMM+AR keeps
+        // them consecutive: its reduction is split over a pair's R units (two-shot).
         const int64_t rs_block = 2 * (int64_t)clusters;
+        const int rs_group = 2;
         if (mode == kModeRS && (int64_t)p->pairs_m * tiles_n >= 3 * rs_block) p->block_tiles = (int)rs_block;
-        p->rank_group = 1;
+        p->rank_group = p->block_tiles > 0 ? std::min(rs_group, R) : 1;
         // caller's order overrides (are_workspace_set_gemm_order); they change the
         // order of the work units only, never the arithmetic
         if (ws->order_group_m > 0) p->group_m = (int)std::min<int64_t>(p->pairs_m, ws->order_group_m);
@@ -262,6 +268,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         } else if (ws->order_block < 0) {
             p->block_tiles = 0;
         }
+        p->cons = ws->d_cons;
         // destination-rotated order (chunked GEMM+RS): needs owner segments of whole pair
         // rows; chunk c of every segment then runs before chunk c+1 of any
         if (p->chunks > 0 && ws->chunk_stripe >= 0 && S % 256 == 0) {
@@ -367,6 +374,7 @@ are_status are_workspace_create(are_ws** out, const are_caps* caps) {
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_part, ws->part_bytes);
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_pieces, ws->piece_words * 4);
         if (e == cudaSuccess) e = cudaMalloc(&ws->d_chunk_ctr, (size_t)caps->R_max * kChunkCap * 8);
+        if (e == cudaSuccess) e = cudaMalloc(&ws->d_cons, ws->mask_words * 4);
         if (e == cudaSuccess)
             e = cudaHostAlloc(reinterpret_cast<void**>(&ws->h_chunk_gen), (size_t)caps->R_max * kChunkCap * 4,
                               cudaHostAllocMapped);

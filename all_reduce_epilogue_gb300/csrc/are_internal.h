@@ -112,6 +112,7 @@ struct GemmParams {
     int pairs_m, num_pair_units;  // CTA-pair kernel: 256-row tile pairs, R units per pair
     int block_tiles;     // CTA-pair kernel: tile pairs per rank block (0 = ranks innermost)
     int rank_group;      // CTA-pair kernel: ranks run together inside a block (1 = rank by rank)
+    uint32_t* cons;      // CTA-pair kernel, GEMM+AR: row-slice readers done per tile (0 between calls)
     int group_m;         // tile raster: rows of tiles (pairs) per group
     // chunked owner-segment completion (GEMM+RS; chunk_ctr == nullptr: off)
     unsigned long long* chunk_ctr;  // [R][kChunkCap] monotonic completion counters

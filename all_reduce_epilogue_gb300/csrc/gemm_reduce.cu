@@ -675,6 +675,8 @@ constexpr uint32_t kIdesc2 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (
 
 struct PUnit {
     int t;        // this CTA's 128x256 tile (row-major tile index)
+    int tp;       // position of the tile pair in the unit order
+    int j;        // position of the unit among its pair's R units (GEMM+AR: the row slice it reduces)
     int tm, tn, r, own;
     bool reducer, valid;
     bool pad;     // padding unit of the last rank block: skipped by every role
@@ -708,6 +710,8 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
         j = u - tp * p.R;
     }
     const int num_pairs = p.pairs_m * p.tiles_n;
+    U.tp = tp;
+    U.j = j;
     U.pad = tp >= num_pairs;
     if (U.pad) {  // padding unit: no tile
         U.t = 0; U.tm = p.tiles_m; U.tn = 0; U.r = 0; U.own = 0;
@@ -791,6 +795,12 @@ __device__ __forceinline__ bool grp_bar_or(bool v) {
     return r != 0;
 }
 
+// Partial slot of rank r for this CTA's 128x256 tile: every tile has its own
+// slot per rank in the workspace.
+__device__ __forceinline__ uint8_t* pair_slot(const GemmParams& p, const PUnit& U, int r) {
+    return p.part + ((size_t)r * p.num_tiles + U.t) * kTilePartBytes;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -845,6 +855,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         // ------------------------------------------------------------ TMA producer (both CTAs)
         // The whole warp runs the loop (uniform operands); one elected lane issues.
         const bool issuer = ptx::elect_one();
+        // A panels are reused by every tile column of a raster group: keep them in L2 ahead of
+        // the B panels, which the group's pair rows share only while they run together
+        const uint64_t pol_a = ptx::policy_evict_last();
         const uint64_t pol = ptx::policy_evict_normal();
         int stage = 0;
         uint32_t ph = 0;
@@ -867,7 +880,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     // both CTAs' copies complete on the leader's full barrier
                     const uint32_t fb = ptx::mapa_shared(ptx::smem_u32(&full[stage]), 0);
                     if (q == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2 * kStageTx2);
-                    ptx::tma_load_2d_pair(sA + stage * kAHalfBytes, &p.tmA[U.r], fb, kb * kBK, U.tm * kBM, pol);
+                    ptx::tma_load_2d_pair(sA + stage * kAHalfBytes, &p.tmA[U.r], fb, kb * kBK, U.tm * kBM, pol_a);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         ptx::tma_load_2d_pair(sB + stage * kBHalfBytes + h * 8192, &p.tmB[U.r], fb,
@@ -964,7 +977,9 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 const int u = i * G2 + (cl + i) % G2;
                 if (u >= p.num_pair_units) continue;
                 const PUnit U = decode_pair(p, MODE, u, (int)q);
-                if (!U.reducer || !U.valid) continue;
+                // GEMM+RS: the tile's reducer (its owner) loads all of it; GEMM+AR: every unit
+                // loads its row slice
+                if (!U.valid || (MODE == kModeRS && !U.reducer)) continue;
                 bool ok = true;
                 uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
                 if (seen != full_mask) {
@@ -991,16 +1006,35 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (!ok) break;
                 // generic-proxy acquire above, async-proxy (bulk copy) reads below
                 ptx::fence_proxy_async_global();
-                for (int j = 0; j < 2 * nsub && ok; ++j) {
-                    for (int r = 0; r < p.R; ++r) {
-                        if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(&pfull[ps], kPSub2);
-                        const uint8_t* src =
-                            p.part + ((size_t)r * p.num_tiles + U.t) * kTilePartBytes + (size_t)j * kPSub2;
-                        ptx::bulk_load(sP + ps * kPSub2, src, kPSub2, &pfull[ps]);
-                        issued |= 1u << ps;
-                        issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
-                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                if (MODE == kModeAR) {
+                    // row slice U.j: groups of up to 16 rows; a stage holds one rank's group,
+                    // 1 KB per 64-byte column sub-tile (sub-tile st at st * 1 KB)
+                    const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
+                    for (int g0 = lo; g0 < hi && ok; g0 += 16) {
+                        const int nr = min(16, hi - g0);
+                        for (int r = 0; r < p.R; ++r) {
+                            if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
+                            ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(2 * nsub * nr * 64));
+                            const uint8_t* src = pair_slot(p, U, r) + (size_t)g0 * 64;
+                            for (int st = 0; st < 2 * nsub; ++st)
+                                ptx::bulk_load(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
+                                               (uint32_t)(nr * 64), &pfull[ps]);
+                            issued |= 1u << ps;
+                            issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        }
+                    }
+                } else {
+                    for (int j = 0; j < 2 * nsub && ok; ++j) {
+                        for (int r = 0; r < p.R; ++r) {
+                            if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
+                            ptx::mbar_arrive_expect_tx(&pfull[ps], kPSub2);
+                            const uint8_t* src = pair_slot(p, U, r) + (size_t)j * kPSub2;
+                            ptx::bulk_load(sP + ps * kPSub2, src, kPSub2, &pfull[ps]);
+                            issued |= 1u << ps;
+                            issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        }
                     }
                 }
                 if (!ok) break;
@@ -1030,7 +1064,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             if (grp_bar_or<1>(bad)) { bad = true; break; }
             ptx::tc_fence_after();
             const uint32_t tacc = tmem_base + lane_base + buf * kBN;
-            uint8_t* gdst = p.part + ((size_t)U.r * p.num_tiles + U.t) * kTilePartBytes;
+            uint8_t* gdst = pair_slot(p, U, U.r);
             if (U.valid) {
                 for (int j = 0; j < nsub; ++j) {
                     uint32_t w[32];
@@ -1103,11 +1137,86 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             const int u = i * G2 + (cl + i) % G2;
             if (u >= p.num_pair_units) continue;
             const PUnit U = decode_pair(p, MODE, u, (int)q);
-            if (!U.reducer || !U.valid) continue;
+            if (MODE == kModeAR && !U.pad && U.valid) {
+                // ---- GEMM+AR: this unit reduces row slice U.j of its tile (a two-shot all-reduce:
+                // rank j sums slice j of all R partials in the order r = 0..R-1, then writes it
+                // to every view), so every unit of a pair takes 1/R of the tile's reduction
+                const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
+                const int st = row >> 4, rr = row & 15;  // 64-byte column sub-tile, row in the group
+                const int wq = warp - 8;
+                for (int g0 = lo; g0 < hi; g0 += 16) {
+                    const int nr = min(16, hi - g0);
+                    const int trow = g0 + rr;  // tile row of this thread
+                    float acc[32];
+                    for (int qq = 0; qq < p.R; ++qq) {
+                        if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
+                        uint32_t v[16];
+                        if (rr < nr) {
+                            const uint8_t* rp = sP + ps * kPSub2 + st * 1024 + rr * 64;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                const uint4 x = *reinterpret_cast<const uint4*>(rp + ((c ^ ((trow >> 1) & 3)) << 4));
+                                v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] = 0u;
+                        }
+                        ptx::mbar_arrive(&pempty[ps]);
+                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        if (qq == 0) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                acc[2 * e] = __uint_as_float(v[e] << 16);
+                                acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
+                                acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
+                            }
+                        }
+                    }
+                    // stage the group's bf16 rows (16 x 512 bytes; 16-byte chunk k of row rr at
+                    // position k ^ rr), then write every view with whole-row 16-byte stores.
+                    // The barrier also orders the previous group's reads of the staging buffer.
+                    if (grp_bar_or<2>(bad)) { bad = true; break; }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4*>(sOut + rr * 512 + (((st * 4 + c) ^ rr) << 4)) =
+                            make_uint4(pack_bf16x2(acc[8 * c], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                                       pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]),
+                                       pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+                    grp_bar<2>();
+                    const int gcol = U.tn * kBN + lane * 8;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int orr = wq + 4 * i;
+                        const int grow = U.tm * kBM + g0 + orr;
+                        if (orr < nr && grow < p.M && gcol < p.N) {
+                            const uint4 val = *reinterpret_cast<const uint4*>(sOut + orr * 512 + ((lane ^ orr) << 4));
+                            for (int w = 0; w < p.nviews; ++w)
+                                ptx::st_stream_v4(p.views[w] + (size_t)grow * p.N + gcol, val);
+                        }
+                    }
+                }
+                if (bad) break;
+                if (lead && lane == 0) {
+                    // the last of the tile's R slice reducers re-arms its mask word (and this count)
+                    const uint32_t old = atomicAdd(&p.cons[U.t], 1u);
+                    if (old == (uint32_t)p.R - 1u) {
+                        atomicExch(&p.cons[U.t], 0u);
+                        if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
+                    }
+                }
+                continue;
+            }
+            if (MODE == kModeAR || !U.reducer || !U.valid) continue;
             const int row0 = U.tm * kBM;
             for (int c = 0; c < kBN / 64; ++c) {  // 64-column output chunks
                 uint32_t outw[32];
-                if (MODE == kModeRS) {
+                {
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {  // partial sub-tile 4c + h: columns 16h..16h+15 of the chunk
                         float acc[16];
@@ -1128,83 +1237,25 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 #pragma unroll
                         for (int e = 0; e < 8; ++e) outw[8 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
                     }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {  // partial sub-tile 2c + h: columns 32h..32h+31 of the chunk
-                        float acc[32];
-                        for (int qq = 0; qq < p.R; ++qq) {
-                            uint32_t v[16];  // 32 bf16
-                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
-                            read_row_sw64(sP + ps * kPSub2, row, v);
-                            ptx::mbar_arrive(&pempty[ps]);
-                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
-                            if (qq == 0) {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    acc[2 * e] = __uint_as_float(v[e] << 16);
-                                    acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
-                                    acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) outw[16 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
-                    }
                 }
                 const int sb = 0;  // one staging buffer: lane 0 issues and waits for its stores
-                if (MODE == kModeRS && lead && lane == 0) ptx::bulk_wait_read0();
+                if (lead && lane == 0) ptx::bulk_wait_read0();
                 if (grp_bar_or<2>(bad)) { bad = true; break; }
                 write_row_sw128(sOut, row, outw);
-                if (MODE == kModeAR) {
-                    // every view gets the chunk through coalesced 16-byte stores: thread t moves
-                    // 16-byte column chunk t mod 8 of rows t/8 + 16i, so a warp writes four whole
-                    // 128-byte row segments per store.  The TMA engine stays free for the
-                    // mainloop's operand loads (R views of TMA stores measured 17% slower).
-                    grp_bar<2>();
-                    const int x = U.tn * kBN + c * 64;
-                    const int cc = row & 7;
-                    const int gcol = x + cc * 8;
-                    uint4 v[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int r = (row >> 3) + 16 * i;
-                        v[i] = *reinterpret_cast<const uint4*>(sOut + r * 128 + ((cc ^ (r & 7)) << 4));
-                    }
-                    if (gcol < p.N) {
-                        for (int w = 0; w < p.nviews; ++w) {
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int grow = row0 + (row >> 3) + 16 * i;
-                                if (grow < p.M) ptx::st_stream_v4(p.views[w] + (size_t)grow * p.N + gcol, v[i]);
-                            }
-                        }
-                    }
-                    continue;  // the next chunk's barrier orders these reads before sOut is rewritten
-                }
                 ptx::fence_proxy_async_shared();
                 grp_bar<2>();
                 if (lead && lane == 0) {
                     const int x = U.tn * kBN + c * 64;
                     if (x < p.N) {
-                        if (MODE == kModeRS) {
-                            // owner-boundary flush: one store per (segment piece, H-row box)
-                            const int row_end = min(row0 + kBM, p.M);
-                            for (int r0 = row0; r0 < row_end;) {
-                                const int s = r0 / p.S;
-                                const int e = min((s + 1) * p.S, row_end);
-                                for (int rb = r0; rb < e; rb += p.H)
-                                    ptx::tma_store_2d(&p.tmOut[s], sOut + sb * kSubBytes + (rb - row0) * 128, x,
-                                                      rb - s * p.S);
-                                r0 = e;
-                            }
-                        } else {
-                            for (int v = 0; v < p.nviews; ++v)
-                                ptx::tma_store_2d(&p.tmOut[v], sOut + sb * kSubBytes, x, row0);
+                        // owner-boundary flush: one store per (segment piece, H-row box)
+                        const int row_end = min(row0 + kBM, p.M);
+                        for (int r0 = row0; r0 < row_end;) {
+                            const int s = r0 / p.S;
+                            const int e = min((s + 1) * p.S, row_end);
+                            for (int rb = r0; rb < e; rb += p.H)
+                                ptx::tma_store_2d(&p.tmOut[s], sOut + sb * kSubBytes + (rb - row0) * 128, x,
+                                                  rb - s * p.S);
+                            r0 = e;
                         }
                         ptx::bulk_commit();
                     }

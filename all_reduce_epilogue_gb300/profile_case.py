@@ -29,6 +29,8 @@ def main(argv=None) -> int:
     ap.add_argument("--path", choices=["default", "oneshot", "lamport"], default="default",
                     help="allreduce_rmsnorm: force a kernel")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--order", default="", help="gemm: group_m,block_pairs,rank_group (0 = default)")
+    ap.add_argument("--chunks", type=int, default=0, help="gemm_rs: chunks per owner segment (rotated order)")
     a = ap.parse_args(argv)
     torch.manual_seed(a.seed)
     dev = torch.device("cuda", 0)
@@ -51,6 +53,10 @@ def main(argv=None) -> int:
         A = [bf(a.M, a.K, scale=s) for _ in range(a.R)]
         B = [bf(a.K, a.N, scale=s) for _ in range(a.R)]
         with are.Workspace(R_max=a.R, M_max=a.M, N_max=a.N, K_max=a.K) as ws:
+            if a.order:
+                ws.set_gemm_order(*[int(v) for v in a.order.split(",")])
+            if a.chunks:
+                ws.set_chunks(a.chunks, 0)
             if a.op == "gemm_rs":
                 out = torch.empty(a.M, a.N, dtype=torch.bfloat16, device=dev)
                 for _ in range(a.iters):

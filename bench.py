@@ -159,7 +159,7 @@ def peak_regime(clocks) -> tuple:
 CLOCK_QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-CLOCK_PERIOD_MS = 20
+CLOCK_PERIOD_MS = int(os.environ.get("ARE_CLOCK_PERIOD_MS", "20"))
 
 
 class ClockSampler:
@@ -388,11 +388,13 @@ CONFIGS = [
 ]
 
 
-def time_calls(calls, dev, replays: int = 3):
+def time_calls(calls, dev, replays: int = 3, idle_s: float = 0.1):
     """Capture the callables `calls` (one library call each, on the current
     stream) in one CUDA graph, replay it once untimed, then `replays` times
-    timed with CUDA events on the replay stream.  Returns the per-call times
-    (us) of the replays."""
+    timed with CUDA events on the replay stream, each after `idle_s` seconds
+    idle so that every replay starts at the burst clock (a replay of several
+    milliseconds of GEMMs right after another one runs under the power cap).
+    Returns the per-call times (us) of the replays."""
     import torch
     s = torch.cuda.Stream(dev)
     s.wait_stream(torch.cuda.current_stream(dev))
@@ -409,6 +411,7 @@ def time_calls(calls, dev, replays: int = 3):
     torch.cuda.synchronize(dev)
     out = []
     for _ in range(replays):
+        time.sleep(idle_s)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(cur)
@@ -632,29 +635,27 @@ def run_gpu(args):
     per_ms = {p: statistics.mean(v) for p, v in per.items()}
 
     # AR+RMSNorm alone, back to back: the Lamport kernel the step runs (inside the
-    # step it runs at the clock the power cap leaves while the GEMMs run), and the
-    # one-shot kernel on the same workload (forced; the default dispatch sends this
-    # size to the Lamport kernel).  Reported beside the step, not part of it.
+    # step it runs after the GEMMs, which leave dirty lines in L2 and, over long runs,
+    # a power-capped clock), and the one-shot kernel on the same workload (forced; the
+    # default dispatch sends this size to the Lamport kernel).  A CUDA graph of calls,
+    # replayed, so that no host stall between launches shows up as GPU time.
+    # Reported beside the step, not part of it.
     def alone(flags):
         ws.set_debug(flags)
-        for _ in range(args.warmup):
-            are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
-        o0 = torch.cuda.Event(enable_timing=True)
-        o1 = torch.cuda.Event(enable_timing=True)
-        n_alone = max(args.steps, 20)
-        o0.record(stream)
-        for _ in range(n_alone):
-            are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws, stream)
-        o1.record(stream)
-        torch.cuda.synchronize(dev)
+        n_alone = 20
+        us = time_calls([lambda: are.allreduce_rmsnorm(P_n, res_n, gamma_n, EPS, out_n, ws)] * n_alone, dev)
         ws.set_debug(0)
         st = ws.device_status()
         if st["code"] != 0:
             raise RuntimeError(f"device status after AR+RMSNorm alone ({flags}): {st}")
-        return max_over_ranks(dist, o0.elapsed_time(o1) / n_alone, dev)
+        return max_over_ranks(dist, statistics.median(us) * 1e-3, dev)
 
+    wa0 = time.time()
     lamport_alone_ms = alone(0)
+    windows["lamport_alone"] = (wa0, time.time())
+    wa0 = time.time()
     oneshot_ms = alone(are.DEBUG_AR_ONESHOT)
+    windows["oneshot_alone"] = (wa0, time.time())
 
     # every workload at every size, one by one (after the step; outside its timed region)
     cfg_windows = []
@@ -698,7 +699,9 @@ def run_gpu(args):
                    "note": f"of {source}; in the step"}
     ach_alone = bytes_n / (lamport_alone_ms * 1e-3) / 1e9
     roofline_ar["alone"] = {"ms": lamport_alone_ms, "achieved": ach_alone, "frac": ach_alone / peaks["hbm_gbs"],
-                            "note": "the same kernel, calls back to back outside the step (inputs larger than L2)"}
+                            "clock_mhz_median": sampler.summary(windows["lamport_alone"]).get("sm_mhz"),
+                            "note": "the same kernel outside the step: CUDA graph of 20 calls, median of 3 replays "
+                                    "(inputs larger than L2)"}
     flops_ar, _ = work("gemm_ar")
     ach_ga = flops_ar / (per_ms["gemm_ar"] * 1e-3) / 1e12
     roofline_gemm_ar = {"kernel": "gemm_pair_kernel<AR> (gemm_ar)", "bound": "tensor", "achieved": ach_ga,
@@ -819,6 +822,8 @@ def run_gpu(args):
             "allreduce_rmsnorm_oneshot": {
                 "kernel": "ar_oneshot_kernel<4> (same workload, path forced; outside the step)",
                 "ms": oneshot_ms, "gbs_algorithmic": work("allreduce_rmsnorm")[1] / (oneshot_ms * 1e-3) / 1e9,
+                "timing": "CUDA graph of 20 calls, median of 3 replays",
+                "clock_mhz_median": sampler.summary(windows["oneshot_alone"]).get("sm_mhz"),
                 "frac": work("allreduce_rmsnorm")[1] / (oneshot_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                 "vs_lamport_in_step": per_ms["allreduce_rmsnorm"] / oneshot_ms},
             "cpu_baseline": cpu,

@@ -257,11 +257,13 @@ ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t byte
  *  block_pairs : > 0: tile pairs are taken in blocks of block_pairs, and a
  *                block's units run in rank groups (below); < 0: the R units of
  *                a tile pair run consecutively; 0 = the library's choice
- *                (GEMM+RS with at least three blocks of two waves of pairs:
- *                blocks of two waves, rank by rank; otherwise consecutive).
+ *                (GEMM+RS with at least 6 x (co-resident clusters) tile pairs:
+ *                blocks of two waves of pairs in rank groups of 2; otherwise
+ *                consecutive).
  *  rank_group  : with block_pairs > 0, the number of ranks whose units of a
  *                block run together (1 = rank by rank, R = a pair's R units
- *                consecutive); 0 = 1.
+ *                consecutive); 0 = 1.  With block_pairs = 0 the library's
+ *                choice is used for both.
  * Returns ARE_EINVAL for negative group_m / rank_group or rank_group > 8. */
 ARE_API are_status are_workspace_set_gemm_order(are_ws* ws, int group_m, int block_pairs, int rank_group);
 
