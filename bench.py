@@ -775,6 +775,18 @@ def run_gpu(args):
 
     e2e_step()
     torch.cuda.synchronize(dev)
+    # the host link on its own, just before: one step's input copies alone (pinned host ->
+    # device, one stream), so the e2e figure can be read against the link it ran on (the host
+    # memory and its link are shared with other jobs on the machine)
+    l0 = torch.cuda.Event(enable_timing=True)
+    l1 = torch.cuda.Event(enable_timing=True)
+    l0.record(s_in)
+    for ins, _, _ in parts_io:
+        for h, d in ins:
+            d.view(torch.int16).copy_(h, non_blocking=True)
+    l1.record(s_in)
+    torch.cuda.synchronize(dev)
+    link_h2d_gbs = (h2d - hgamma.numel() * 4) / (l0.elapsed_time(l1) * 1e-3) / 1e9
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -830,7 +842,8 @@ def run_gpu(args):
             "clocks": clocks,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "steps": e2e_steps,
-                    "overlap": "host->device copies, the calls and device->host copies on three streams"},
+                    "overlap": "host->device copies, the calls and device->host copies on three streams",
+                    "link_h2d_gbs": link_h2d_gbs},
             "gpu_launches": 3 * args.steps,
             "peaks": {"source": source, "regime": regime, **peaks},
         }
