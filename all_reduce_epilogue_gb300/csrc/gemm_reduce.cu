@@ -747,10 +747,20 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
         U.tn = in / gm;
     }
     U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
-    int r = U.own + 1 + j;
-    while (r >= p.R) r -= p.R;
+    int r;
+    if (p.rot_pc > 0) {
+        // rotated order: a wave holds pairs of every owner segment, so every pair runs its
+        // ranks in the same order 0..R-1 (a wave then streams the operands of the same one or
+        // two ranks whatever the owners) and the owner's unit is not last.  Its reducer then
+        // waits for later units; they never wait on a reduction, so that wait ends too.
+        r = j;
+    } else {
+        // the owner's unit last, so its reducer finds the peers' partials already published
+        r = U.own + 1 + j;
+        while (r >= p.R) r -= p.R;
+    }
     U.r = r;
-    U.reducer = (j == p.R - 1);
+    U.reducer = (r == U.own);
     U.tm = 2 * tmp + q;
     U.valid = U.tm < p.tiles_m;
     U.t = U.tm * p.tiles_n + U.tn;

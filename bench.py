@@ -383,7 +383,8 @@ CONFIGS = [
     ("allreduce_rmsnorm R=8", "allreduce_rmsnorm", 8, [1, 16, 128, 1024, 4096], 7168, 0, 3, "normal", 0),
     ("large gemm_rs R=8", "gemm_rs", 8, [8192], 8192, 4096, 4, "normal", 0),
     # the same with chunked owner-segment completion (8 chunks per segment) and the
-    # destination-rotated tile order: the cost of the counters and of the order
+    # destination-rotated tile order striped every 4 tile columns: the cost of the
+    # counters and of the order
     ("large gemm_rs R=8, chunked + rotated", "gemm_rs", 8, [8192], 8192, 4096, 4, "normal", 8),
 ]
 
@@ -485,7 +486,7 @@ def run_configs(ws, dev, dev_step, peaks, sampler_windows):
                                  torch.empty((M, N), dtype=torch.bfloat16, device=dev)))
             for path in paths:
                 ws.set_debug({"default": 0, "oneshot": are.DEBUG_AR_ONESHOT, "lamport": are.DEBUG_AR_LAMPORT}[path])
-                ws.set_chunks(chunks, 0)
+                ws.set_chunks(chunks, 4)
                 kernels = []
                 if op == "allreduce_rmsnorm":
                     def mk(st):
