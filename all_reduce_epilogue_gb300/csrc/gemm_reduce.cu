@@ -748,11 +748,13 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
     }
     U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
     int r;
-    if (p.rot_pc > 0) {
+    if (p.rot_pc > 0 || mode == kModeAR) {
         // rotated order: a wave holds pairs of every owner segment, so every pair runs its
         // ranks in the same order 0..R-1 (a wave then streams the operands of the same one or
         // two ranks whatever the owners) and the owner's unit is not last.  Its reducer then
         // waits for later units; they never wait on a reduction, so that wait ends too.
+        // GEMM+AR: every unit reduces a row slice once all R units have published, so no
+        // unit has to come last either.
         r = j;
     } else {
         // the owner's unit last, so its reducer finds the peers' partials already published
