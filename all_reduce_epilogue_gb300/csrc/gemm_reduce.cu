@@ -663,10 +663,11 @@ constexpr int kPairThreads = 384;
 constexpr uint32_t kAHalfBytes = kBM * kBK * 2;      // 16 KB: 128 rows of A
 constexpr uint32_t kBHalfBytes = (kBN / 2) * kBK * 2;  // 16 KB: 128 columns of B (two 64x64 boxes)
 constexpr uint32_t kStageTx2 = kAHalfBytes + kBHalfBytes;
-constexpr int kNumBars2 = 2 * kStages2 + 2 * kAccBufs2 + 2 * kPStages2 + 1;
-// A/B stages, partial buffer, one reduce staging buffer, two drain staging buffers
+constexpr int kNumBars2 = 2 * kStages2 + 2 * kAccBufs2 + 2 * kPStages2 + 1 + 2;
+// A/B stages, partial buffer, one reduce staging buffer, two drain staging buffers, one 8 KB buffer
+// that with the reduce staging buffer's second half holds GEMM+AR's own row slices
 constexpr size_t kSmemBytes2 = 1024 + (size_t)kStages2 * (kAHalfBytes + kBHalfBytes) +
-                               (size_t)kPStages2 * kPSub2 + (size_t)kSubBytes + 2 * (size_t)kPSub2 +
+                               (size_t)kPStages2 * kPSub2 + (size_t)kSubBytes + 3 * (size_t)kPSub2 +
                                kNumBars2 * 8 + 16;
 static_assert(kSmemBytes2 <= 232448, "shared memory budget (pair)");
 // D fp32, A/B bf16, A K-major, B MN-major, N = 256, M = 256 (pair).
@@ -822,19 +823,35 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     uint8_t* sP = sB + kStages2 * kBHalfBytes;
     uint8_t* sOut = sP + kPStages2 * kPSub2;     // reduce staging (1 buffer)
     uint8_t* sDrain = sOut + kSubBytes;          // drain staging (2 buffers of kPSub2)
-    uint64_t* full = reinterpret_cast<uint64_t*>(sDrain + 2 * kPSub2);
+    // GEMM+AR at R = 8: a unit's own 16-row slice (8 sub-tiles x 16 rows x 64 bytes) stays on chip
+    uint8_t* const sOwn0 = sOut + kPSub2;
+    uint8_t* const sOwn1 = sDrain + 2 * kPSub2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sDrain + 3 * kPSub2);
     uint64_t* empty = full + kStages2;
     uint64_t* tfull = empty + kStages2;
     uint64_t* tempty = tfull + kAccBufs2;
     uint64_t* pfull = tempty + kAccBufs2;
     uint64_t* pempty = pfull + kPStages2;
     uint64_t* mma_done = pempty + kPStages2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    uint64_t* ownfree = mma_done + 1;           // [2]: the reduce has read an own-slice buffer
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ownfree + 2);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t q = ptx::cluster_ctarank();  // 0 = leader
+    // GEMM+AR with 16-row slices (R = 8): unit j's rank is j (every pair runs ranks 0..R-1), so the
+    // slice it reduces, rows [16j, 16j+16), of its own partial never needs to leave the SM: the drain
+    // keeps those rows in sOwn instead of storing them, and the slice reducer adds them at rank j's
+    // place in the ring-order sum.  That saves 1/R of the partial exchange's writes and reads.
+    // With two sOwn buffers the drain of a CTA's n-th valid unit waits for the reduction of its
+    // (n-2)-th, the one place where a drain waits on a reduction.  That wait ends when a pair's R
+    // units lie within two consecutive steps of the persistent loop (the units of a pair consecutive,
+    // and at least R - 1 clusters): the reduction at step m then needs drains at steps <= m + 1
+    // only, so by induction over the steps every wait ends.  Rank-blocked orders spread a pair over
+    // up to R steps, so there the own slice goes through memory like the other ranks' slices.
+    const bool own_slice = (MODE == kModeAR) && p.R == 8 && (p.block_tiles == 0 || p.rank_group >= p.R) &&
+                           p.rot_pc == 0 && (int)(gridDim.x >> 1) >= p.R - 1;
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
     const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row
@@ -844,6 +861,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         for (int s = 0; s < kAccBufs2; ++s) { ptx::mbar_init(&tfull[s], 1); ptx::mbar_init(&tempty[s], 2); }
         for (int s = 0; s < kPStages2; ++s) { ptx::mbar_init(&pfull[s], 1); ptx::mbar_init(&pempty[s], 128); }
         ptx::mbar_init(mma_done, 1);
+        for (int s = 0; s < 2; ++s) ptx::mbar_init(&ownfree[s], 1);
         *abort_flag = 0u;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_shared();
@@ -1025,6 +1043,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     for (int g0 = lo; g0 < hi && ok; g0 += 16) {
                         const int nr = min(16, hi - g0);
                         for (int r = 0; r < p.R; ++r) {
+                            if (own_slice && r == U.j) continue;  // on chip (sOwn)
                             if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
                             ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(2 * nsub * nr * 64));
                             const uint8_t* src = pair_slot(p, U, r) + (size_t)g0 * 64;
@@ -1062,6 +1081,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         const bool lead = (warp == 4) && (lane == 0);
         const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_u32(&tempty[0]), 0);
         int it = 0;
+        int nvalid = 0;         // valid units drained: own-slice buffer nvalid & 1
         bool bad = false;
         uint64_t w_tfull = 0;
         for (int i = 0;; ++i) {
@@ -1078,6 +1098,14 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             const uint32_t tacc = tmem_base + lane_base + buf * kBN;
             uint8_t* gdst = pair_slot(p, U, U.r);
             if (U.valid) {
+                const int olo = U.j * 16, ohi = olo + 16;  // own slice rows (own_slice only)
+                const int oslot = nvalid & 1;
+                uint8_t* const own_buf = oslot ? sOwn1 : sOwn0;
+                if (own_slice && nvalid >= 2) {
+                    // the buffer's previous slice (two valid units ago) must have been read
+                    const bool ok = wait_bar(&ownfree[oslot], (uint32_t)((nvalid >> 1) - 1) & 1u, abort_flag, p, 16, u, 200);
+                    if (grp_bar_or<1>(!ok)) { bad = true; break; }
+                }
                 for (int j = 0; j < nsub; ++j) {
                     uint32_t w[32];
                     __syncwarp();
@@ -1102,6 +1130,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     // the 128-byte row chunk becomes partial sub-tiles 2j and 2j+1: swizzled smem
                     // staging -> one 8 KB bulk store each; staging buffer b belongs to lane b,
                     // which waits only for its own bulk group before refilling it
+                    if (own_slice && row >= olo && row < ohi) {
+                        // the own slice's rows of sub-tiles 2j, 2j+1, laid out as a loaded stage
+                        write_half_sw64<0>(own_buf + (2 * j) * 1024 - olo * 64, row, w);
+                        write_half_sw64<1>(own_buf + (2 * j + 1) * 1024 - olo * 64, row, w);
+                    }
                     if (warp == 4 && lane < 2) ptx::bulk_wait_read0();
                     grp_bar<1>();
                     write_half_sw64<0>(sDrain, row, w);
@@ -1109,10 +1142,18 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     ptx::fence_proxy_async_shared();
                     grp_bar<1>();
                     if (warp == 4 && lane < 2) {
-                        ptx::bulk_store(gdst + (size_t)(2 * j + lane) * kPSub2, sDrain + lane * kPSub2, kPSub2);
+                        uint8_t* dst = gdst + (size_t)(2 * j + lane) * kPSub2;
+                        const uint8_t* src = sDrain + lane * kPSub2;
+                        if (own_slice) {  // every row but the own slice's
+                            if (olo > 0) ptx::bulk_store(dst, src, (uint32_t)(olo * 64));
+                            if (ohi < kBM) ptx::bulk_store(dst + ohi * 64, src + ohi * 64, (uint32_t)((kBM - ohi) * 64));
+                        } else {
+                            ptx::bulk_store(dst, src, kPSub2);
+                        }
                         ptx::bulk_commit();
                     }
                 }
+                ++nvalid;
                 // publish once this tile's partial is in memory: only the two issuing lanes wait
                 if (warp == 4) {
                     if (lane < 2) {
@@ -1140,6 +1181,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         const int row = threadIdx.x - 256;
         const bool lead = (warp == 8);
         int prev_tm = -1;  // chunk counting: the last reducer tile whose stores may still be in flight
+        int nvalid = 0;    // GEMM+AR: valid units reduced (own-slice buffer nvalid & 1, as in the drain)
         int ps = 0;
         uint32_t pph = 0;
         bool bad = false;
@@ -1156,15 +1198,24 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
                 const int st = row >> 4, rr = row & 15;  // 64-byte column sub-tile, row in the group
                 const int wq = warp - 8;
+                const int oslot = nvalid & 1;
+                const uint8_t* const own_buf = oslot ? sOwn1 : sOwn0;
                 for (int g0 = lo; g0 < hi; g0 += 16) {
                     const int nr = min(16, hi - g0);
                     const int trow = g0 + rr;  // tile row of this thread
                     float acc[32];
                     for (int qq = 0; qq < p.R; ++qq) {
-                        if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
+                        const bool mine = own_slice && qq == U.j;
+                        // The own slice was written by this CTA's drain before it published the unit's
+                        // mask bit; the loader acquired the full mask before filling this unit's stages,
+                        // so a wait on one of them orders those writes first.  For rank 0 that is the
+                        // wait on the next stage (rank 1's, not consumed here); for a later rank the
+                        // waits on the stages before it already did.
+                        if (!mine || qq == 0)
+                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
                         uint32_t v[16];
                         if (rr < nr) {
-                            const uint8_t* rp = sP + ps * kPSub2 + st * 1024 + rr * 64;
+                            const uint8_t* rp = (mine ? own_buf : sP + ps * kPSub2) + st * 1024 + rr * 64;
 #pragma unroll
                             for (int c = 0; c < 4; ++c) {
                                 const uint4 x = *reinterpret_cast<const uint4*>(rp + ((c ^ ((trow >> 1) & 3)) << 4));
@@ -1174,8 +1225,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
 #pragma unroll
                             for (int e = 0; e < 16; ++e) v[e] = 0u;
                         }
-                        ptx::mbar_arrive(&pempty[ps]);
-                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        if (!mine) {
+                            ptx::mbar_arrive(&pempty[ps]);
+                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        }
                         if (qq == 0) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
@@ -1194,6 +1247,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     // position k ^ rr), then write every view with whole-row 16-byte stores.
                     // The barrier also orders the previous group's reads of the staging buffer.
                     if (grp_bar_or<2>(bad)) { bad = true; break; }
+                    // every read of the own slice is done: hand its buffer back to the drain
+                    if (own_slice && lead && lane == 0) ptx::mbar_arrive(&ownfree[oslot]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         *reinterpret_cast<uint4*>(sOut + rr * 512 + (((st * 4 + c) ^ rr) << 4)) =
@@ -1222,6 +1277,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
                     }
                 }
+                ++nvalid;
                 continue;
             }
             if (MODE == kModeAR || !U.reducer || !U.valid) continue;

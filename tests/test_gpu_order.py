@@ -82,3 +82,38 @@ def test_orders_with_chunks_and_rotation(oracle):
         used = oracle.chunk_pieces(R, M, N, C) > 0
         assert np.array_equal(ws.chunk_counters()[:R, :C], np.where(used, 3 << 32, 0).astype(np.uint64))
         check_close(host_f32(out), oracle.gemm_rs(A, B), "orders + chunks + rotation")
+
+
+@pytest.mark.parametrize("order", [(0, 76, 1), (0, 76, 2), (2, 38, 8), (0, -1, 0)])
+def test_ar_rank_blocks_spanning_many_steps(order):
+    """GEMM+AR at R = 8 keeps a unit's own row slice on chip only while a
+    pair's units lie within two steps of the persistent loop; a rank-blocked
+    order that spreads a pair over up to R steps (blocks of 76 pairs, ranks in
+    groups of 1 or 2) must run through memory instead, with no expired wait
+    and the same bytes as the one-CTA kernel (whole-tile reduction in the same
+    rank order) and the library's own order."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    R, M, N, K = 8, 4096, 2560, 128  # 160 tile pairs, 1280 units: many steps of 76 clusters
+    A, B = synth.gemm_inputs(R, M, N, K, 4242)
+    Ad, Bd = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros_like(ref)
+    with are.Workspace(R_max=8, M_max=M, N_max=N, K_max=K) as ws:
+        ws.set_debug(are.DEBUG_SINGLE_CTA)
+        are.gemm_ar(Ad, Bd, ref, ws)
+        assert ws.device_status()["code"] == 0
+        ws.set_debug(are.DEBUG_PAIR_CTA)
+        are.gemm_ar(Ad, Bd, out, ws)
+        assert ws.device_status()["code"] == 0
+        assert np.array_equal(host_bits(out), host_bits(ref))
+        ws.set_gemm_order(*order)
+        for _ in range(2):
+            out.zero_()
+            are.gemm_ar(Ad, Bd, out, ws)
+            st = ws.device_status()
+            assert st["code"] == 0, (order, st)
+            assert ws.last_launch()["kernel"] == "gemm_pair_kernel"
+            assert np.array_equal(host_bits(out), host_bits(ref)), order
