@@ -200,8 +200,19 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         if (e == cudaSuccess && mode == kModeRS)
             e = make_tmap_bf16(&p->tmOut[r], out[r], (uint64_t)N, (uint64_t)S, 64, (uint32_t)H);
     }
+    // CTA pairs (256-row tiles) wherever there are at least two tile rows and
+    // the device can co-schedule the clusters; one CTA per tile otherwise.
+    const int clusters = ws->pair_clusters;
+    // Below one wave of pairs the reduce of the last (only) wave is the kernel's tail, and
+    // the one-CTA kernel's deeper partial buffer (and its reducer's own partial kept in
+    // TMEM) finishes it sooner: R=4, M=256 measured 33 us against 69 us.
+    const int64_t pair_units = (int64_t)((tiles_m + 1) / 2) * tiles_n * R;
+    const bool pair_ok = tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
+    const bool use_pair = pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA));
+    // GEMM+AR views: the one-CTA kernel stores whole 128-row tiles, the pair kernel 16-row
+    // groups of a unit's row slice (boxes of 64 columns either way)
     for (int v = 0; v < nviews && e == cudaSuccess; ++v) {
-        e = make_tmap_bf16(&p->tmOut[v], views[v], (uint64_t)N, (uint64_t)M, 64, kBM);
+        e = make_tmap_bf16(&p->tmOut[v], views[v], (uint64_t)N, (uint64_t)M, 64, use_pair ? 16u : (uint32_t)kBM);
         p->views[v] = const_cast<are_bf16*>(views[v]);
     }
     if (e != cudaSuccess) {
@@ -236,15 +247,7 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         p->chunk_host = ws->d_chunk_gen;
         p->chunks = ws->chunks;
     }
-    // CTA pairs (256-row tiles) wherever there are at least two tile rows and
-    // the device can co-schedule the clusters; one CTA per tile otherwise.
-    const int clusters = ws->pair_clusters;
-    // Below one wave of pairs the reduce of the last (only) wave is the kernel's tail, and
-    // the one-CTA kernel's deeper partial buffer (and its reducer's own partial kept in
-    // TMEM) finishes it sooner: R=4, M=256 measured 33 us against 69 us.
-    const int64_t pair_units = (int64_t)p->pairs_m * tiles_n * R;
-    const bool pair_ok = tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
-    if (pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA))) {
+    if (use_pair) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
         // GEMM+RS with at least three blocks of two waves of tile pairs: run the ranks block
         // by block, two ranks at a time, so a wave streams the operands of two ranks.  A

@@ -96,8 +96,9 @@ enum GemmMode : int { kModeRS = 0, kModeAR = 1 };
 struct GemmParams {
     CUtensorMap tmA[kMaxRanks];
     CUtensorMap tmB[kMaxRanks];
-    CUtensorMap tmOut[kMaxRanks];
-    are_bf16* views[kMaxRanks];  // GEMM+AR: distinct output views (the pair kernel stores with st.global)
+    CUtensorMap tmOut[kMaxRanks];  // GEMM+RS: owner segments (64 x H boxes); GEMM+AR: the distinct views
+                                   // (64 x 128 boxes for the one-CTA kernel, 64 x 16 for the pair kernel)
+    are_bf16* views[kMaxRanks];  // GEMM+AR: distinct output views (ragged row groups: st.global)
     uint8_t* part;       // [R][T][tile part bytes]
     uint32_t* mask;      // [T]
     DevStatus* status;

@@ -1243,12 +1243,40 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                             }
                         }
                     }
-                    // stage the group's bf16 rows (16 x 512 bytes; 16-byte chunk k of row rr at
-                    // position k ^ rr), then write every view with whole-row 16-byte stores.
-                    // The barrier also orders the previous group's reads of the staging buffer.
+                    // A full group of 16 rows is staged as four 128B-swizzled boxes of 64 columns
+                    // (16 rows x 128 bytes each) and written to every view by TMA tensor stores,
+                    // one box per view and 64 columns.  A ragged group (R not dividing 128) is
+                    // staged as 16 x 512-byte rows (16-byte chunk k of row rr at position k ^ rr)
+                    // and written with whole-row 16-byte stores, so no box covers rows of
+                    // another unit's slice.  The issuing thread waits until the previous group's
+                    // stores have read the staging buffer; the barrier then orders the rewrite.
+                    const bool tma_views = (nr == 16);
+                    if (lead && lane == 0) ptx::bulk_wait_read0();
                     if (grp_bar_or<2>(bad)) { bad = true; break; }
                     // every read of the own slice is done: hand its buffer back to the drain
                     if (own_slice && lead && lane == 0) ptx::mbar_arrive(&ownfree[oslot]);
+                    if (tma_views) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const int k = st * 4 + c;  // 16-byte chunk of the 512-byte row
+                            *reinterpret_cast<uint4*>(sOut + (k >> 3) * 2048 + rr * 128 + (((k & 7) ^ (rr & 7)) << 4)) =
+                                make_uint4(pack_bf16x2(acc[8 * c], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
+                                           pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]),
+                                           pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
+                        }
+                        ptx::fence_proxy_async_shared();
+                        grp_bar<2>();
+                        if (lead && lane == 0) {
+                            const int y = U.tm * kBM + g0;
+                            for (int w = 0; w < p.nviews; ++w)
+#pragma unroll
+                                for (int b = 0; b < 4; ++b)  // boxes past N or M would store nothing
+                                    if (U.tn * kBN + b * 64 < p.N && y < p.M)
+                                        ptx::tma_store_2d(&p.tmOut[w], sOut + b * 2048, U.tn * kBN + b * 64, y);
+                            ptx::bulk_commit();
+                        }
+                        continue;
+                    }
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         *reinterpret_cast<uint4*>(sOut + rr * 512 + (((st * 4 + c) ^ rr) << 4)) =
