@@ -109,6 +109,7 @@ __device__ __forceinline__ void b_bar() {
 struct Shared {
     uint8_t* stage;     // stages x 28 KB
     uint8_t* res;       // kResSlots x N*2 bytes (when the residual is staged in shared memory)
+    float* gam;         // N fp32 (when gamma is staged in shared memory)
     uint64_t* full;     // [stages]
     uint64_t* empty;    // [stages]
     uint64_t* rfull;    // [kResSlots]
@@ -122,7 +123,8 @@ __device__ __forceinline__ Shared carve(uint8_t* base, const ArParams& p) {
     Shared s;
     s.stage = base;
     s.res = base + (size_t)p.stages * kStageBytes;
-    uint8_t* tail = s.res + (p.res_in_smem ? (size_t)kResSlots * p.N * 2 : 0);
+    s.gam = reinterpret_cast<float*>(s.res + (p.res_in_smem ? (size_t)kResSlots * p.N * 2 : 0));
+    uint8_t* tail = reinterpret_cast<uint8_t*>(s.gam) + (p.gamma_in_smem ? (size_t)p.N * 4 : 0);
     tail = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tail) + 15) & ~uintptr_t(15));
     s.full = reinterpret_cast<uint64_t*>(tail);
     s.empty = s.full + kMaxArStages;
@@ -226,17 +228,29 @@ __device__ __forceinline__ float warp_max(float v) {
 // round to nearest even, saturating; both divisions correctly rounded).
 // NT threads hold the row's packs bt, bt + NT, ...; bar() is their barrier and
 // red[16..] their scratch.
+// gamma of pack pk: from the block's shared-memory copy `gsm` when there is one, else
+// from global memory through L1
+__device__ __forceinline__ void gamma8(const ArParams& p, const float* gsm, int pk, float4& g0, float4& g1) {
+    if (gsm) {
+        g0 = reinterpret_cast<const float4*>(gsm)[pk * 2];
+        g1 = reinterpret_cast<const float4*>(gsm)[pk * 2 + 1];
+    } else {
+        g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
+        g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+    }
+}
+
 template <int PPT, int NT, typename Bar>
 __device__ __forceinline__ void store_row(const ArParams& p, int64_t row, int bt, const float (&h)[PPT][8], float inv,
-                                          float* red, Bar bar) {
+                                          float* red, const float* gsm, Bar bar) {
     const int P = p.packs_per_row;
     if (!p.out_q) {
 #pragma unroll
         for (int k = 0; k < PPT; ++k) {
             const int pk = bt + k * NT;
             if (pk < P) {
-                const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
-                const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+                float4 g0, g1;
+                gamma8(p, gsm, pk, g0, g1);
                 uint4 o;
                 o.x = pack_bf16x2(h[k][0] * inv * g0.x, h[k][1] * inv * g0.y);
                 o.y = pack_bf16x2(h[k][2] * inv * g0.z, h[k][3] * inv * g0.w);
@@ -254,8 +268,8 @@ __device__ __forceinline__ void store_row(const ArParams& p, int64_t row, int bt
     for (int k = 0; k < PPT; ++k) {
         const int pk = bt + k * NT;
         if (pk < P) {
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+            float4 g0, g1;
+            gamma8(p, gsm, pk, g0, g1);
             const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
             for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(h[k][i] * inv * g[i]));
@@ -278,8 +292,8 @@ __device__ __forceinline__ void store_row(const ArParams& p, int64_t row, int bt
     for (int k = 0; k < PPT; ++k) {
         const int pk = bt + k * NT;
         if (pk < P) {
-            const float4 g0 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2);
-            const float4 g1 = __ldg(reinterpret_cast<const float4*>(p.gamma) + pk * 2 + 1);
+            float4 g0, g1;
+            gamma8(p, gsm, pk, g0, g1);
             const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
             uint32_t c[8];
 #pragma unroll
@@ -400,7 +414,7 @@ __device__ __forceinline__ void norm_row(const ArParams& p, const Shared& sh, in
         hv[k][4] = __uint_as_float(hi[k].x); hv[k][5] = __uint_as_float(hi[k].y);
         hv[k][6] = __uint_as_float(hi[k].z); hv[k][7] = __uint_as_float(hi[k].w);
     }
-    store_row<PPT, kBThreads>(p, row, bt, hv, inv, sh.red, [] { b_bar(); });
+    store_row<PPT, kBThreads>(p, row, bt, hv, inv, sh.red, p.gamma_in_smem ? sh.gam : nullptr, [] { b_bar(); });
 }
 
 template <int PPT>
@@ -598,6 +612,13 @@ __global__ void __launch_bounds__(kArThreads, 1) ar_rmsnorm_kernel(const __grid_
         uint32_t rph = 0;
         uint64_t w_spin = 0, w_res = 0;
         const uint64_t c_start = clock64();
+        if (p.gamma_in_smem) {
+            // every row reads all of gamma: one copy per block in shared memory instead of
+            // re-reading it through L1 (which this kernel's shared-memory carve-out leaves small)
+            for (int i = bt; i < p.N / 4; i += kBThreads)
+                reinterpret_cast<float4*>(sh.gam)[i] = __ldg(reinterpret_cast<const float4*>(p.gamma) + i);
+            b_bar();
+        }
         for (int c = 0; c < p.num_chunks; ++c) {
             const int64_t row0 = (int64_t)c * p.chunk_rows;
             const int rows = (int)min((int64_t)p.chunk_rows, (int64_t)p.M - row0);
@@ -735,7 +756,7 @@ __global__ void __launch_bounds__(kOsThreads, 1) ar_oneshot_kernel(const __grid_
         }
         __syncthreads();
         const float inv = rsqrtf(red[kOsThreads / 32] * p.inv_n + p.eps);
-        store_row<PPT, kOsThreads>(p, row, bt, h, inv, red, [] { __syncthreads(); });
+        store_row<PPT, kOsThreads>(p, row, bt, h, inv, red, nullptr, [] { __syncthreads(); });
         // red[] is rewritten by the next row; this barrier also keeps the warps together, which
         // measured 10 % faster than letting early warps poll for the next row's copies
         __syncthreads();
@@ -768,6 +789,8 @@ int ar_rmsnorm_ppt(int packs_per_row) {
     return 0;
 }
 
+size_t ar_rmsnorm_smem_bytes(const ArParams& p);
+
 void ar_rmsnorm_smem_plan(ArParams& p) {
     // residual rows in shared memory when three of them leave room for >= 4 stages
     const size_t res_bytes = (size_t)kResSlots * p.N * 2;
@@ -778,10 +801,14 @@ void ar_rmsnorm_smem_plan(ArParams& p) {
     int st = (int)(avail / kStageBytes);
     if (st > kArStages) st = kArStages;
     p.stages = st;
+    // gamma in shared memory when it fits beside the stages and the residual rows
+    p.gamma_in_smem = 0;
+    p.gamma_in_smem = (ar_rmsnorm_smem_bytes(p) + (size_t)p.N * 4 <= kSmemLimit) ? 1 : 0;
 }
 
 size_t ar_rmsnorm_smem_bytes(const ArParams& p) {
-    return (size_t)p.stages * kStageBytes + (p.res_in_smem ? (size_t)kResSlots * p.N * 2 : 0) + kTailBytes;
+    return (size_t)p.stages * kStageBytes + (p.res_in_smem ? (size_t)kResSlots * p.N * 2 : 0) +
+           (p.gamma_in_smem ? (size_t)p.N * 4 : 0) + kTailBytes;
 }
 
 int ar_rmsnorm_resident_blocks(int ppt, int num_sms) {

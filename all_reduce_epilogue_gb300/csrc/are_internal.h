@@ -53,6 +53,7 @@ struct ArParams {
     int ring_slots;     // 0: chunk c's rows at c*chunk_rows; else staging slot c % ring_slots
     int stages;         // phase-A shared-memory stages (set by ar_rmsnorm_smem_plan)
     int res_in_smem;    // residual rows streamed into shared memory (set by ar_rmsnorm_smem_plan)
+    int gamma_in_smem;  // gamma copied into shared memory once per block (set by ar_rmsnorm_smem_plan)
     float eps;
     float inv_n;
     uint32_t flags;
