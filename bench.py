@@ -60,9 +60,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # line reports null.
 KERNEL_SOURCES = {"gemm_rs": "gemm_reduce.cu", "gemm_ar": "gemm_reduce.cu", "allreduce_rmsnorm": "ar_rmsnorm.cu"}
 NCU_TRAFFIC = {
-    "gemm_rs": (10060.8e6, "0c0c9f38eb6e54b1"),
-    "gemm_ar": (2802.9e6, "0c0c9f38eb6e54b1"),
-    "allreduce_rmsnorm": (623.6e6, "d385419471be5a90"),
+    "gemm_rs": (10048.6e6, "00f96c92dd01ac38"),
+    "gemm_ar": (2767.5e6, "00f96c92dd01ac38"),
+    "allreduce_rmsnorm": (626.4e6, "a4af1f7bd1f46c00"),
 }
 
 
