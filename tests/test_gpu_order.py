@@ -117,3 +117,34 @@ def test_ar_rank_blocks_spanning_many_steps(order):
             assert st["code"] == 0, (order, st)
             assert ws.last_launch()["kernel"] == "gemm_pair_kernel"
             assert np.array_equal(host_bits(out), host_bits(ref)), order
+
+
+@pytest.mark.parametrize("R,M,N,K", [(8, 600, 1000, 192), (8, 1300, 264, 128)])
+def test_ar_own_slice_odd_tile_rows_ragged(oracle, R, M, N, K):
+    """GEMM+AR at R = 8 with an odd number of tile rows (the last pair's second
+    CTA has no tile, so the two CTAs of a cluster count their units differently),
+    M not a multiple of 16 (slices past the last row) and ragged N: the pair
+    kernel, which keeps each unit's own row slice on chip and writes the views
+    with TMA tensor stores, gives the one-CTA kernel's bytes and the oracle's
+    values, with no expired wait."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    A, B = synth.gemm_inputs(R, M, N, K, 9000 + M)
+    Ad, Bd = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
+    ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    views = [torch.full((M, N), 3.0, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    with are.Workspace(R_max=8, M_max=M, N_max=N, K_max=K) as ws:
+        ws.set_debug(are.DEBUG_SINGLE_CTA)
+        are.gemm_ar(Ad, Bd, ref, ws)
+        assert ws.device_status()["code"] == 0
+        ws.set_debug(are.DEBUG_PAIR_CTA)
+        for _ in range(2):
+            are.gemm_ar(Ad, Bd, views, ws)
+            st = ws.device_status()
+            assert st["code"] == 0, st
+            assert ws.last_launch()["kernel"] == "gemm_pair_kernel"
+            for v in views:
+                assert np.array_equal(host_bits(v), host_bits(ref))
+    check_close(host_f32(views[0]), oracle.gemm_ar(A, B), f"gemm_ar R={R} M={M} N={N} K={K}")
