@@ -854,12 +854,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     // place in the ring-order sum.  That saves 1/R of the partial exchange's writes and reads.
     // With two sOwn buffers the drain of a CTA's n-th valid unit waits for the reduction of its
     // (n-2)-th, the one place where a drain waits on a reduction.  That wait ends when a pair's R
-    // units lie within two consecutive steps of the persistent loop (the units of a pair consecutive,
-    // and at least R - 1 clusters): the reduction at step m then needs drains at steps <= m + 1
-    // only, so by induction over the steps every wait ends.  Rank-blocked orders spread a pair over
-    // up to R steps, so there the own slice goes through memory like the other ranks' slices.
-    const bool own_slice = (MODE == kModeAR) && p.R == 8 && (p.block_tiles == 0 || p.rank_group >= p.R) &&
-                           p.rot_pc == 0 && (int)(gridDim.x >> 1) >= p.R - 1;
+    // units lie within two consecutive steps of the persistent loop: the reduction at step m then
+    // needs drains at steps <= m + 1 only, so by induction over the steps every wait ends.  A
+    // pair's units lie in a run of `run` consecutive units (R with the ranks consecutive, else the
+    // pair's rank block), and runs start at multiples of `run`; such a run spans at most two steps
+    // when it is at most G + 1 units long, or exactly 2G (then it starts at a step boundary).  Larger
+    // rank blocks spread a pair over more steps, and there the own slice goes through memory like
+    // the other ranks' slices.
+    const int own_run = (p.block_tiles == 0 || p.rank_group >= p.R) ? p.R : p.block_tiles * p.R;
+    const int G2own = (int)(gridDim.x >> 1);
+    const bool own_slice = (MODE == kModeAR) && p.R == 8 && p.rot_pc == 0 &&
+                           (own_run <= G2own + 1 || own_run == 2 * G2own);
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
     const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row

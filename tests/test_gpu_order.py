@@ -84,14 +84,15 @@ def test_orders_with_chunks_and_rotation(oracle):
         check_close(host_f32(out), oracle.gemm_rs(A, B), "orders + chunks + rotation")
 
 
-@pytest.mark.parametrize("order", [(0, 76, 1), (0, 76, 2), (2, 38, 8), (0, -1, 0)])
+@pytest.mark.parametrize("order", [(0, 76, 1), (0, 76, 2), (2, 38, 8), (0, -1, 0), (0, 19, 1), (4, 19, 4), (0, 9, 2)])
 def test_ar_rank_blocks_spanning_many_steps(order):
     """GEMM+AR at R = 8 keeps a unit's own row slice on chip only while a
     pair's units lie within two steps of the persistent loop; a rank-blocked
     order that spreads a pair over up to R steps (blocks of 76 pairs, ranks in
     groups of 1 or 2) must run through memory instead, with no expired wait
     and the same bytes as the one-CTA kernel (whole-tile reduction in the same
-    rank order) and the library's own order."""
+    rank order) and the library's own order.  Blocks of 19 pairs (two waves of
+    76 clusters) or of 9 (under one wave) keep the own slice on chip."""
     need_gpu()
     import torch
 
