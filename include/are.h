@@ -56,6 +56,13 @@
  *    of that call are undefined and the workspace must be re-armed with
  *    are_workspace_reset() before further use (until then every call aborts
  *    at its first wait).
+ *  - The GEMM kernels and the Lamport AR+RMSNorm kernel run persistent grids
+ *    no larger than what the device holds at once (co-resident CTA clusters,
+ *    resp. blocks), and their waits on other CTAs' work assume that the whole
+ *    grid runs together.  Kernels of other streams that occupy SMs at the
+ *    same time can delay part of the grid; a wait that then expires ends the
+ *    call with an error status as above, never with a hang.  For full speed,
+ *    and to stay clear of that, run these calls without concurrent kernels.
  */
 #ifndef ARE_H
 #define ARE_H
