@@ -294,7 +294,11 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         e = launch_gemm_pair(*p, mode, grid, s);
     } else {
         p->group_m = (int)std::min<int64_t>(tiles_m, 8);
-        const int grid = (int)std::min<int64_t>(p->num_units, ws->num_sms);
+        // as many CTAs as keep every one busy for the same number of units: with more units
+        // than SMs, the last wave no longer runs on a fraction of the SMs while the rest idle
+        // (streaming-bound problems then keep the full DRAM bandwidth to the end)
+        const int64_t waves = ceil_div(p->num_units, (int64_t)ws->num_sms);
+        const int grid = (int)ceil_div(p->num_units, waves);
         ws->last = are_launch_info{ARE_KERNEL_GEMM_ONE_CTA, grid, kGemmThreads, 1, 0, 0, R, p->group_m};
         e = launch_gemm_reduce(*p, mode, grid, s);
     }
