@@ -393,14 +393,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
                     ptx::fence_proxy_async_global();
                 }
                 if (!ok) break;
+                // only the tile's rows inside M were stored (128-byte rows, a sub-tile's row r at r * 128)
+                const uint32_t vbytes = (uint32_t)min(kBM, p.M - U.tm * kBM) * 128u;
                 for (int j = 0; j < nsub && ok; ++j) {
                     for (int q = 0; q < p.R; ++q) {
                         if (q == U.own) continue;
                         if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 3, u)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(&pfull[ps], kSubBytes);
+                        ptx::mbar_arrive_expect_tx(&pfull[ps], vbytes);
                         const uint8_t* src =
                             p.part + ((size_t)q * p.num_tiles + U.t) * kTilePartBytes + (size_t)j * kSubBytes;
-                        ptx::bulk_load(sP + ps * kSubBytes, src, kSubBytes, &pfull[ps]);
+                        ptx::bulk_load(sP + ps * kSubBytes, src, vbytes, &pfull[ps]);
                         issued |= 1u << ps;
                         issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
                         if (++ps == kPStages) { ps = 0; pph ^= 1u; }
@@ -435,7 +437,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 
             if (!U.reducer) {
                 // ---- producer unit: TMEM -> registers -> swizzled smem -> bulk store -> publish
+                // (a sub-tile's rows past M are never read: only the rows inside M are stored)
                 uint8_t* gdst = p.part + ((size_t)U.r * p.num_tiles + U.t) * kTilePartBytes;
+                const uint32_t vbytes = (uint32_t)min(kBM, p.M - row0) * 128u;
                 for (int j = 0; j < nsub; ++j) {
                     uint32_t w[32];
                     if (MODE == kModeRS) {
@@ -461,7 +465,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
                     ptx::fence_proxy_async_shared();
                     epi_bar();
                     if (lead && lane == sb) {
-                        ptx::bulk_store(gdst + (size_t)j * kSubBytes, sOut + sb * kSubBytes, kSubBytes);
+                        ptx::bulk_store(gdst + (size_t)j * kSubBytes, sOut + sb * kSubBytes, vbytes);
                         ptx::bulk_commit();
                     }
                 }
