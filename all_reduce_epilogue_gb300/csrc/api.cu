@@ -201,13 +201,17 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
             e = make_tmap_bf16(&p->tmOut[r], out[r], (uint64_t)N, (uint64_t)S, 64, (uint32_t)H);
     }
     // CTA pairs (256-row tiles) wherever there are at least two tile rows and
-    // the device can co-schedule the clusters; one CTA per tile otherwise.
+    // the device can co-schedule the clusters; one CTA per tile otherwise.  GEMM+AR
+    // also takes the pairs with a single tile row (the pair's second tile does not
+    // exist, as with any odd number of tile rows): such a problem is bound by streaming
+    // B, and the pair kernel spreads the reduction over a pair's R units and keeps every
+    // SM streaming (R=8, M=64, N=7168, K=2048: 58.6 against 64.5 us).
     const int clusters = ws->pair_clusters;
     // Below one wave of pairs the reduce of the last (only) wave is the kernel's tail, and
     // the one-CTA kernel's deeper partial buffer (and its reducer's own partial kept in
     // TMEM) finishes it sooner: R=4, M=256 measured 33 us against 69 us.
     const int64_t pair_units = (int64_t)((tiles_m + 1) / 2) * tiles_n * R;
-    const bool pair_ok = tiles_m >= 2 && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
+    const bool pair_ok = (tiles_m >= 2 || mode == kModeAR) && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
     const bool use_pair = pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA));
     // GEMM+AR views: the one-CTA kernel stores whole 128-row tiles, the pair kernel 16-row
     // groups of a unit's row slice (boxes of 64 columns either way)

@@ -31,7 +31,8 @@ def _gemm(op, R, M, N, K, flags=0):
     ("rs", 4, 256, 4096, 2048, "gemm_reduce_kernel"),   # below one wave of pairs
     ("rs", 4, 8192, 4096, 2048, "gemm_pair_kernel"),
     ("rs", 8, 8192, 8192, 4096, "gemm_pair_kernel"),
-    ("ar", 8, 64, 7168, 2048, "gemm_reduce_kernel"),
+    ("ar", 8, 64, 7168, 2048, "gemm_pair_kernel"),     # one tile row: the pair's second tile is empty
+    ("ar", 8, 1, 1000, 128, "gemm_reduce_kernel"),     # below one wave of pairs
     ("ar", 8, 4096, 7168, 2048, "gemm_pair_kernel"),
     ("rs", 2, 64, 256, 0, "memset"),
 ])
