@@ -3,6 +3,7 @@ import numpy as np
 import pytest
 
 import oracle
+import oracle as oracle_mod
 from oracle import check_close
 import synth
 from tests.gpu_util import dev_bf16, host_bits, host_f32, need_gpu, sample_rows
@@ -180,6 +181,40 @@ def test_unpublished_tile_times_out_and_reset_recovers(oracle, single_cta):
         ws.reset()
         got = host_f32(run_rs(ws, A, B))
     check_close(got, oracle.gemm_rs(A, B), "after reset")
+
+
+def test_gemm_ar_unpublished_unit_times_out_with_own_slice(oracle):
+    """GEMM+AR at R = 8 through the CTA-pair kernel, where each unit keeps its
+    own row slice on chip and a drain waits for the reduction two units back:
+    when unit 0 never publishes, every slice reducer of that tile pair times out
+    on the mask, the drains waiting on those reductions give up with the abort,
+    every CTA returns with a timeout status, and a reset recovers the workspace
+    (the next call matches the oracle)."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    R, M, N, K = 8, 512, 512, 128
+    A, B = synth.gemm_inputs(R, M, N, K, 18)
+    dA, dB = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
+    views = [torch.empty((M, N), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    with make_ws(timeout_ns=20_000_000) as ws:
+        ws.set_debug(are.DEBUG_PAIR_CTA | are.DEBUG_SKIP_PUBLISH, 0)
+        are.gemm_ar(dA, dB, views, ws)
+        st = ws.device_status()
+        assert st["status"] == are.ETIMEOUT and st["code"] in (are.DEV_MASK_TIMEOUT, are.DEV_PIPE_TIMEOUT), st
+        assert ws.last_launch()["kernel"] == "gemm_pair_kernel"
+        ws.set_debug(are.DEBUG_PAIR_CTA)
+        ws.reset()
+        are.gemm_ar(dA, dB, views, ws)
+        assert ws.device_status()["code"] == 0
+        ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws.set_debug(are.DEBUG_SINGLE_CTA)
+        are.gemm_ar(dA, dB, ref, ws)
+        assert ws.device_status()["code"] == 0
+    for v in views:  # after the reset: the one-CTA kernel's bytes, and the oracle's values
+        assert np.array_equal(host_bits(v), host_bits(ref))
+    assert oracle_mod.rel_l2(host_f32(ref), oracle.gemm_ar(A, B)) <= 2e-3
 
 
 def test_k_zero_and_empty(oracle):
