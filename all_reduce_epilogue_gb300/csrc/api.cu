@@ -253,19 +253,32 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     }
     if (use_pair) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
-        // GEMM+RS with at least three blocks of two waves of tile pairs: run the ranks block
-        // by block, two ranks at a time, so a wave streams the operands of two ranks.  A
-        // block's reductions all come at its end.  Measured (us per call): the large GEMM+RS
-        // 2662 with blocks of two waves and rank groups of 2, against 2691 with half-wave
-        // blocks rank by rank, 2717 with two-wave blocks rank by rank and 3000 with a pair's
-        // R units consecutive; R=4, M=8192, N=4096, K=2048: 401 against 397 consecutive and
-        // 465 with half-wave blocks.  Below the threshold a block's reduction burst is not
-        // hidden and the ranks stay consecutive (R=4, M=4096: 213 against 220).  GEMM+AR keeps
-        // them consecutive: its reduction is split over a pair's R units (two-shot).
-        const int64_t rs_block = 2 * (int64_t)clusters;
-        const int rs_group = 2;
-        if (mode == kModeRS && (int64_t)p->pairs_m * tiles_n >= 3 * rs_block) p->block_tiles = (int)rs_block;
-        p->rank_group = p->block_tiles > 0 ? std::min(rs_group, R) : 1;
+        const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
+        if (mode == kModeRS && !p->chunk_ctr) {
+            // GEMM+RS pushes a running sum along the ranks (rank r adds its accumulator to rank
+            // r-1's sum), so a tile's rank r+1 should run after its rank r: one block of all the
+            // tile pairs, rank by rank (each rank sweeps every tile in raster order, as one GEMM
+            // would), with raster groups of 8 pair rows.  No padding, and with at least a wave
+            // of pairs a tile's consecutive ranks are never in the same wave.  Measured on the
+            // large GEMM+RS (us per call, one box): 2361 against 2362 (blocks of 256 pairs), 2373
+            // (128), 2417 (76 = one wave, 320 padding units), 2452 (152), 2430 (4 pair-row raster)
+            // and 4831 with a pair's ranks consecutive (each tile's drains then wait in a chain).
+            p->block_tiles = (int)num_pairs;
+            p->rank_group = 1;
+            p->group_m = (int)std::min<int64_t>(p->pairs_m, 8);
+        } else if (mode == kModeRS) {
+            // chunked GEMM+RS gathers every rank's partial at the tile's owner: with at least
+            // three blocks of two waves of tile pairs, run the ranks block by block, two at a
+            // time, so a wave streams the operands of two ranks; below that a block's reduction
+            // burst is not hidden and the ranks stay consecutive.
+            const int64_t rs_block = 2 * (int64_t)clusters;
+            if (num_pairs >= 3 * rs_block) {
+                p->block_tiles = (int)rs_block;
+                p->rank_group = std::min(2, R);
+            }
+        }
+        // GEMM+AR keeps a pair's R units consecutive: its reduction is split over them (two-shot).
+        if (p->block_tiles == 0) p->rank_group = 1;
         // caller's order overrides (are_workspace_set_gemm_order); they change the
         // order of the work units only, never the arithmetic
         if (ws->order_group_m > 0) p->group_m = (int)std::min<int64_t>(p->pairs_m, ws->order_group_m);

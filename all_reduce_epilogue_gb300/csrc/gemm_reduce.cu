@@ -761,7 +761,8 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
     }
     U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
     int r;
-    if (p.rot_pc > 0 || mode == kModeAR) {
+    const bool ring = (mode == kModeRS) && p.chunk_ctr == nullptr && p.rot_pc == 0;
+    if (p.rot_pc > 0 || mode == kModeAR || ring) {
         // rotated order: a wave holds pairs of every owner segment, so every pair runs its
         // ranks in the same order 0..R-1 (a wave then streams the operands of the same one or
         // two ranks whatever the owners) and the owner's unit is not last.  Its reducer then
@@ -775,7 +776,7 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
         while (r >= p.R) r -= p.R;
     }
     U.r = r;
-    U.reducer = (r == U.own);
+    U.reducer = !ring && (r == U.own);  // the push ring (GEMM+RS) has no gathering reducer
     U.tm = 2 * tmp + q;
     U.valid = U.tm < p.tiles_m;
     U.t = U.tm * p.tiles_n + U.tn;
@@ -872,6 +873,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
     const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row
+    const bool ring = (MODE == kModeRS) && p.chunk_ctr == nullptr && p.rot_pc == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
@@ -1024,6 +1026,47 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 const int u = i * G2 + (cl + i) % G2;
                 if (u >= p.num_pair_units) continue;
                 const PUnit U = decode_pair(p, MODE, u, (int)q);
+                if (ring) {
+                    // push ring: rank r > 0 streams S_(r-1), the running sum rank r-1 published
+                    if (!U.valid || U.r == 0) continue;
+                    const uint32_t bit = 1u << (U.r - 1);
+                    bool ok = true;
+                    uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
+                    if (!(seen & bit)) {
+                        const uint64_t c0 = clock64();
+                        const uint64_t t0 = ptx::globaltimer();
+                        while (true) {
+                            ptx::nanosleep(100);
+                            seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
+                            if (seen & bit) break;
+                            if (*abort_flag || ptx::ld_relaxed_gpu(&p.status->code) != 0u) {
+                                *abort_flag = 1u;
+                                ok = false;
+                                break;
+                            }
+                            if (ptx::globaltimer() - t0 > p.timeout_ns) {
+                                record_error(p.status, ARE_DEV_MASK_TIMEOUT, blockIdx.x, U.t, (int32_t)seen);
+                                *abort_flag = 1u;
+                                ok = false;
+                                break;
+                            }
+                        }
+                        w_mask += (uint64_t)(clock64() - c0);
+                    }
+                    if (!ok) break;
+                    ptx::fence_proxy_async_global();
+                    const uint8_t* src = pair_slot(p, U, U.r - 1);
+                    for (int st = 0; st < 2 * nsub && ok; ++st) {
+                        if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&pfull[ps], kPSub2);
+                        ptx::bulk_load(sP + ps * kPSub2, src + (size_t)st * kPSub2, kPSub2, &pfull[ps]);
+                        issued |= 1u << ps;
+                        issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                    }
+                    if (!ok) break;
+                    continue;
+                }
                 // GEMM+RS: the tile's reducer (its owner) loads all of it; GEMM+AR: every unit
                 // loads its row slice
                 if (!U.valid || (MODE == kModeRS && !U.reducer)) continue;
@@ -1099,6 +1142,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         const uint32_t tempty_leader = ptx::mapa_shared(ptx::smem_u32(&tempty[0]), 0);
         int it = 0;
         int nvalid = 0;         // valid units drained: own-slice buffer nvalid & 1
+        int dps = 0;            // push ring: partial-buffer stage this drain reads next, and its parity
+        uint32_t dpph = 0;
         bool bad = false;
         uint64_t w_tfull = 0;
         for (int i = 0;; ++i) {
@@ -1123,6 +1168,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     const bool ok = wait_bar(&ownfree[oslot], (uint32_t)((nvalid >> 1) - 1) & 1u, abort_flag, p, 16, u, 200);
                     if (grp_bar_or<1>(!ok)) { bad = true; break; }
                 }
+                // push ring (GEMM+RS): rank r > 0 adds S_(r-1), streamed into the partial buffer by
+                // the loader in sub-tile order, to its accumulator: S_r = S_(r-1) + P_r; the last
+                // rank writes bf16(S_(R-1)) to the owners instead of a partial
+                const bool ring_add = ring && U.r > 0;
+                const bool ring_last = ring && U.r == p.R - 1;
+                const int row0 = U.tm * kBM;
+                uint32_t outw[32];
                 for (int j = 0; j < nsub; ++j) {
                     uint32_t w[32];
                     __syncwarp();
@@ -1143,6 +1195,54 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         ptx::tc_fence_before();
                         grp_bar<1>();
                         if (lead) ptx::mbar_arrive_cluster(tempty_leader + (uint32_t)(buf * 8));
+                    }
+                    if (MODE == kModeRS && ring_add) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {  // sub-tile 2j + h: columns 16h..16h+15 of w
+                            uint32_t v[16];
+                            if (!wait_bar(&pfull[dps], dpph, abort_flag, p, 17, u, 200)) bad = true;
+                            read_row_sw64(sP + dps * kPSub2, row, v);
+                            ptx::mbar_arrive(&pempty[dps]);
+                            if (++dps == kPStages2) { dps = 0; dpph ^= 1u; }
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                w[16 * h + e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(w[16 * h + e]));
+                        }
+                    }
+                    if (MODE == kModeRS && ring_last) {
+                        // bf16 of 32 columns: half of the 64-column output chunk j / 2
+                        if (!(j & 1)) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                outw[e] = pack_bf16x2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                outw[16 + e] = pack_bf16x2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));
+                            // one staging buffer: lane 0 of warp 4 issues the chunk's stores and waits for
+                            // their reads before the next chunk is staged
+                            if (warp == 4 && lane == 0) ptx::bulk_wait_read0();
+                            if (grp_bar_or<1>(bad)) { bad = true; break; }
+                            write_row_sw128(sOut, row, outw);
+                            ptx::fence_proxy_async_shared();
+                            grp_bar<1>();
+                            if (warp == 4 && lane == 0) {
+                                const int x = U.tn * kBN + (j >> 1) * 64;
+                                if (x < p.N) {
+                                    // owner-boundary flush: one store per (segment piece, H-row box)
+                                    const int row_end = min(row0 + kBM, p.M);
+                                    for (int r0 = row0; r0 < row_end;) {
+                                        const int s = r0 / p.S;
+                                        const int e = min((s + 1) * p.S, row_end);
+                                        for (int rb = r0; rb < e; rb += p.H)
+                                            ptx::tma_store_2d(&p.tmOut[s], sOut + (rb - row0) * 128, x, rb - s * p.S);
+                                        r0 = e;
+                                    }
+                                    ptx::bulk_commit();
+                                }
+                            }
+                        }
+                        continue;
                     }
                     // the 128-byte row chunk becomes partial sub-tiles 2j and 2j+1: swizzled smem
                     // staging -> one 8 KB bulk store each; staging buffer b belongs to lane b,
@@ -1171,8 +1271,29 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     }
                 }
                 ++nvalid;
-                // publish once this tile's partial is in memory: only the two issuing lanes wait
-                if (warp == 4) {
+                if (MODE == kModeRS && ring && grp_bar_or<1>(bad)) { bad = true; break; }
+                if (MODE == kModeRS && ring_last) {
+                    // the tile is complete: every earlier rank's bit was read by this unit's loader
+                    // before it streamed S_(R-2), so the word can be re-armed now
+                    if (warp == 4 && lane == 0) {
+                        if (p.flags & ARE_DEBUG_LOG_PIECES) {
+                            int32_t* log = p.pieces + (size_t)U.t * kPieceWords;
+                            const int row_end = min(row0 + kBM, p.M);
+                            int n = 0;
+                            for (int r0 = row0; r0 < row_end && n < (kPieceWords - 3) / 3;) {
+                                const int s = r0 / p.S;
+                                const int e = min((s + 1) * p.S, row_end);
+                                log[3 + 3 * n] = s; log[4 + 3 * n] = r0; log[5 + 3 * n] = e;
+                                ++n;
+                                r0 = e;
+                            }
+                            log[0] = U.tm; log[1] = U.tn; log[2] = n;
+                        }
+                        if (p.flags & ARE_DEBUG_NO_REARM) ptx::red_release_or(&p.mask[U.t], 1u << U.r);
+                        else atomicExch(&p.mask[U.t], 0u);
+                    }
+                } else if (warp == 4) {
+                    // publish once this tile's partial is in memory: only the two issuing lanes wait
                     if (lane < 2) {
                         ptx::bulk_wait0();
                         ptx::fence_proxy_async_global();
