@@ -645,23 +645,25 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 // columns of B (32 KB per k-block, 5 stages) and holds its 128x256 half of the
 // accumulator in its own TMEM; the leader (cluster rank 0) issues the MMAs.
 // Each CTA's half is one 128x256 output tile with its own mask word and
-// partial slot; the pair computes the same rank r for both halves, and the
-// pair's reducer rank (owner of the pair's first row for GEMM+RS, pair index
-// mod R for GEMM+AR) reduces both halves.
+// partial slot; the pair computes the same rank r for both halves.
 //
-// The epilogue is split so that no reduction ever holds TMEM:
+// The epilogue:
 //   warps 4-7   drain: TMEM -> registers -> swizzled staging -> 8 KB bulk
-//               stores into the unit's partial slot (fp32 for RS, bf16 for
-//               AR; the reducer's own partial too); the accumulator goes back
-//               to the MMA as soon as it is read, and the unit's bit is
-//               release-ORed once the two issuing lanes' stores completed;
-//   warps 8-11  reduce (reducer units only): sum the R partial tiles in the
-//               order r = 0..R-1 from the 3-stage partial buffer (fed by the
-//               loader warp once the tile's word is (1 << R) - 1), round to
-//               bf16 and store 64-column chunks with TMA per owner piece (RS)
-//               or per view (AR) from one staging buffer.
-// Producers therefore never wait on a reduction, and the MMA never waits on
-// the partial exchange.
+//               stores into the unit's partial slot; the accumulator goes
+//               back to the MMA as soon as it is read, and the unit's bit is
+//               release-ORed once the two issuing lanes' stores completed.
+//               GEMM+RS pushes a running sum along the ranks: rank r's drain
+//               first adds S_(r-1) (fed by the loader warp into the 3-stage
+//               partial buffer once bit r-1 is set) and stores S_r; the last
+//               rank rounds to bf16 and stores the owner pieces with TMA.
+//               GEMM+AR stores bf16 partials (at R = 8 without its own row
+//               slice, which stays in shared memory);
+//   warps 8-11  reduce: GEMM+AR's two-shot all-reduce (every unit sums its row
+//               slice of the R partials in the order r = 0..R-1 and writes it
+//               to every view) and chunked GEMM+RS's gather at the tile's
+//               reducer, both fed by the loader warp.
+// The drain never waits on a reduction (apart from GEMM+AR's bounded
+// own-slice wait, see the kernel), and the MMA never waits on the exchange.
 // ============================================================================
 constexpr int kStages2 = 5;
 constexpr int kPStages2 = 3;
@@ -763,12 +765,14 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
     int r;
     const bool ring = (mode == kModeRS) && p.chunk_ctr == nullptr && p.rot_pc == 0;
     if (p.rot_pc > 0 || mode == kModeAR || ring) {
-        // rotated order: a wave holds pairs of every owner segment, so every pair runs its
-        // ranks in the same order 0..R-1 (a wave then streams the operands of the same one or
-        // two ranks whatever the owners) and the owner's unit is not last.  Its reducer then
-        // waits for later units; they never wait on a reduction, so that wait ends too.
-        // GEMM+AR: every unit reduces a row slice once all R units have published, so no
-        // unit has to come last either.
+        // GEMM+RS on the push ring: rank r adds its accumulator to rank r-1's sum, so a tile's
+        // ranks run in the order 0..R-1 and each waits only for the unit before it.
+        // Rotated order (chunked GEMM+RS): a wave holds pairs of every owner segment, so every
+        // pair runs its ranks in the same order 0..R-1 (a wave then streams the operands of the
+        // same one or two ranks whatever the owners) and the owner's unit is not last.  Its
+        // reducer then waits for later units; they never wait on a reduction, so that wait
+        // ends too.  GEMM+AR: every unit reduces a row slice once all R units have published,
+        // so no unit has to come last either.
         r = j;
     } else {
         // the owner's unit last, so its reducer finds the peers' partials already published
