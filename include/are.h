@@ -260,13 +260,17 @@ ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t byte
  * order decides when each destination's data completes.
  *  group_m     : 256-row tile pairs per raster group (tile pairs are taken
  *                column by column inside a group of group_m pair rows);
- *                0 = the library's choice (4).
+ *                0 = the library's choice (8 for GEMM+RS, 4 otherwise).
  *  block_pairs : > 0: tile pairs are taken in blocks of block_pairs, and a
  *                block's units run in rank groups (below); < 0: the R units of
- *                a tile pair run consecutively; 0 = the library's choice
- *                (GEMM+RS with at least 6 x (co-resident clusters) tile pairs:
- *                blocks of two waves of pairs in rank groups of 2; otherwise
- *                consecutive).
+ *                a tile pair run consecutively; 0 = the library's choice.
+ *                GEMM+RS pushes a running sum from rank to rank, so it runs
+ *                one block of all tile pairs, rank by rank (a pair's R units
+ *                consecutive would make each tile's ranks wait on one another
+ *                in turn).  Chunked GEMM+RS (are_workspace_set_chunks) with at
+ *                least 6 x (co-resident clusters) tile pairs: blocks of two
+ *                waves of pairs in rank groups of 2, else consecutive.
+ *                GEMM+AR: consecutive.
  *  rank_group  : with block_pairs > 0, the number of ranks whose units of a
  *                block run together (1 = rank by rank, R = a pair's R units
  *                consecutive); 0 = 1.  With block_pairs = 0 the library's
