@@ -115,7 +115,7 @@ typedef struct are_caps {
 /* Debug switches (default off; they change bookkeeping, never the arithmetic). */
 enum {
     ARE_DEBUG_NO_REARM = 1u,      /* keep tile masks / staging words as the call left them (snapshots) */
-    ARE_DEBUG_LOG_PIECES = 2u,    /* record the owner pieces each GEMM+RS reducer stored */
+    ARE_DEBUG_LOG_PIECES = 2u,    /* record the owner pieces stored for each GEMM+RS tile */
     ARE_DEBUG_COUNT_CANON = 4u,   /* count staged words canonicalised from -0.0 to +0.0 */
     ARE_DEBUG_SKIP_PUBLISH = 8u,  /* GEMM: work unit `debug_arg` never sets its ready bit */
     ARE_DEBUG_SKIP_STAGE = 16u,   /* AR+RMSNorm: 8-element pack `debug_arg` is never staged */
@@ -124,8 +124,8 @@ enum {
                                      to the counters (see ARE_SNAP_COUNTERS) */
     ARE_DEBUG_AR_ONESHOT = 128u,  /* AR+RMSNorm: take the one-shot path whatever the size (where a row fits) */
     ARE_DEBUG_AR_LAMPORT = 256u,  /* AR+RMSNorm: take the Lamport path whatever the size */
-    ARE_DEBUG_PAIR_CTA = 512u     /* GEMM: use the CTA-pair kernel wherever it applies (two or more tile rows),
-                                     also below one wave of pairs */
+    ARE_DEBUG_PAIR_CTA = 512u     /* GEMM: use the CTA-pair kernel wherever it applies (two or more tile rows;
+                                     GEMM+AR also one), also below one wave of pairs */
 };
 
 /* Device status word, see are_get_device_status(). */
