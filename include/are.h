@@ -138,7 +138,8 @@ typedef struct are_dev_status {
 
 enum {
     ARE_DEV_OK = 0,
-    ARE_DEV_MASK_TIMEOUT = 1,  /* a GEMM reducer waited too long for a tile's ready bits */
+    ARE_DEV_MASK_TIMEOUT = 1,  /* a GEMM unit waited too long for a tile's ready bit(s) (a reducer, or the
+                                  next rank of the GEMM+RS ring) */
     ARE_DEV_STAGE_TIMEOUT = 2, /* an RMSNorm consumer waited too long for a staged pack */
     ARE_DEV_PIPE_TIMEOUT = 3   /* a GEMM pipeline barrier wait expired */
 };
