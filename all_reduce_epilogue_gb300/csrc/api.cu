@@ -254,41 +254,6 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     if (use_pair) {
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
         const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
-        if (mode == kModeRS && !p->chunk_ctr) {
-            // GEMM+RS pushes a running sum along the ranks (rank r adds its accumulator to rank
-            // r-1's sum), so a tile's rank r+1 should run after its rank r: one block of all the
-            // tile pairs, rank by rank (each rank sweeps every tile in raster order, as one GEMM
-            // would), with raster groups of 8 pair rows.  No padding, and with at least a wave
-            // of pairs a tile's consecutive ranks are never in the same wave.  Measured on the
-            // large GEMM+RS (us per call, one box): 2361 against 2362 (blocks of 256 pairs), 2373
-            // (128), 2417 (76 = one wave, 320 padding units), 2452 (152), 2430 (4 pair-row raster)
-            // and 4831 with a pair's ranks consecutive (each tile's drains then wait in a chain).
-            p->block_tiles = (int)num_pairs;
-            p->rank_group = 1;
-            p->group_m = (int)std::min<int64_t>(p->pairs_m, 8);
-        } else if (mode == kModeRS) {
-            // chunked GEMM+RS gathers every rank's partial at the tile's owner: with at least
-            // three blocks of two waves of tile pairs, run the ranks block by block, two at a
-            // time, so a wave streams the operands of two ranks; below that a block's reduction
-            // burst is not hidden and the ranks stay consecutive.
-            const int64_t rs_block = 2 * (int64_t)clusters;
-            if (num_pairs >= 3 * rs_block) {
-                p->block_tiles = (int)rs_block;
-                p->rank_group = std::min(2, R);
-            }
-        }
-        // GEMM+AR keeps a pair's R units consecutive: its reduction is split over them (two-shot).
-        if (p->block_tiles == 0) p->rank_group = 1;
-        // caller's order overrides (are_workspace_set_gemm_order); they change the
-        // order of the work units only, never the arithmetic
-        if (ws->order_group_m > 0) p->group_m = (int)std::min<int64_t>(p->pairs_m, ws->order_group_m);
-        if (ws->order_block > 0) {
-            p->block_tiles = ws->order_block;
-            p->rank_group = ws->order_rank_group > 0 ? std::min(ws->order_rank_group, R) : 1;
-        } else if (ws->order_block < 0) {
-            p->block_tiles = 0;
-        }
-        p->cons = ws->d_cons;
         // destination-rotated order (chunked GEMM+RS): needs owner segments of whole pair
         // rows; chunk c of every segment then runs before chunk c+1 of any
         if (p->chunks > 0 && ws->chunk_stripe >= 0 && S % 256 == 0) {
@@ -300,8 +265,43 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
             p->rot_pc = ps / cs;
             p->rot_w = ws->chunk_stripe > 0 ? std::min<int>(ws->chunk_stripe, (int)tiles_n) : (int)tiles_n;
         }
+        if (mode == kModeRS) {
+            // GEMM+RS pushes a running sum along the ranks (rank r adds its accumulator to rank
+            // r-1's sum), so a tile's rank r+1 should run after its rank r: rank by rank over
+            // blocks of tile pairs (each rank sweeps the block's tiles, as one GEMM would).
+            p->ring = 1;
+            p->rank_group = 1;
+            if (!p->chunk_ctr) {
+                // one block of all the tile pairs, raster groups of 8 pair rows: no padding, and
+                // with at least a wave of pairs a tile's consecutive ranks are never in the same
+                // wave.  Measured on the large GEMM+RS (us per call, one box): 2361 against 2362
+                // (blocks of 256 pairs), 2373 (128), 2417 (76 = one wave, 320 padding units), 2452
+                // (152), 2430 (4 pair-row raster) and 4831 with a pair's ranks consecutive (each
+                // tile's drains then wait in a chain).
+                p->block_tiles = (int)num_pairs;
+                p->group_m = (int)std::min<int64_t>(p->pairs_m, 8);
+            } else {
+                // chunked GEMM+RS completes chunks early: blocks that finish whole chunks, one
+                // order chunk of every segment each in the destination-rotated order, else two
+                // waves of tile pairs of the raster
+                p->block_tiles = p->rot_pc > 0 ? (int)((int64_t)R * p->rot_pc * tiles_n)
+                                               : (int)std::min<int64_t>(num_pairs, 2 * (int64_t)clusters);
+            }
+        } else {
+            // GEMM+AR keeps a pair's R units consecutive: its reduction is split over them (two-shot)
+            p->rank_group = 1;
+        }
+        // caller's order overrides (are_workspace_set_gemm_order); they change the
+        // order of the work units only, never the arithmetic
+        if (ws->order_group_m > 0) p->group_m = (int)std::min<int64_t>(p->pairs_m, ws->order_group_m);
+        if (ws->order_block > 0) {
+            p->block_tiles = ws->order_block;
+            p->rank_group = ws->order_rank_group > 0 ? std::min(ws->order_rank_group, R) : 1;
+        } else if (ws->order_block < 0) {
+            p->block_tiles = 0;
+        }
+        p->cons = ws->d_cons;
         if (p->block_tiles > 0) {
-            const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
             const int64_t blocks = (num_pairs + p->block_tiles - 1) / p->block_tiles;
             p->num_pair_units = (int)(blocks * p->block_tiles * R);
         }

@@ -763,7 +763,7 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
     }
     U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
     int r;
-    const bool ring = (mode == kModeRS) && p.chunk_ctr == nullptr && p.rot_pc == 0;
+    const bool ring = p.ring != 0;
     if (p.rot_pc > 0 || mode == kModeAR || ring) {
         // GEMM+RS on the push ring: rank r adds its accumulator to rank r-1's sum, so a tile's
         // ranks run in the order 0..R-1 and each waits only for the unit before it.
@@ -877,7 +877,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
     const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row
-    const bool ring = (MODE == kModeRS) && p.chunk_ctr == nullptr && p.rot_pc == 0;
+    const bool ring = (MODE == kModeRS) && p.ring != 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
@@ -1148,6 +1148,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         int nvalid = 0;         // valid units drained: own-slice buffer nvalid & 1
         int dps = 0;            // push ring: partial-buffer stage this drain reads next, and its parity
         uint32_t dpph = 0;
+        int prev_tm = -1;       // chunk counting: the last tile whose owner stores may still be in flight
         bool bad = false;
         uint64_t w_tfull = 0;
         for (int i = 0;; ++i) {
@@ -1295,6 +1296,17 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         }
                         if (p.flags & ARE_DEBUG_NO_REARM) ptx::red_release_or(&p.mask[U.t], 1u << U.r);
                         else atomicExch(&p.mask[U.t], 0u);
+                        if (p.chunk_ctr) {
+                            // count the previous tile's pieces once its stores have completed: at most
+                            // this tile's store groups (one per 64-column chunk) may still be pending
+                            if (prev_tm >= 0) {
+                                const int rem_cols = p.N - U.tn * kBN;
+                                ptx::bulk_wait_upto(min(kBN / 64, (rem_cols + 63) / 64));
+                                ptx::fence_proxy_async_global();
+                                chunk_bump_tile(p, prev_tm);
+                            }
+                            prev_tm = U.tm;
+                        }
                     }
                 } else if (warp == 4) {
                     // publish once this tile's partial is in memory: only the two issuing lanes wait
@@ -1318,6 +1330,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
         if (bad) *abort_flag = 1u;
         if (lead) prof_add(p, 5, w_tfull);
         if (warp == 4 && lane < 2) ptx::bulk_wait0();
+        if (MODE == kModeRS && p.chunk_ctr && warp == 4 && lane == 0 && prev_tm >= 0 && !bad) {
+            ptx::fence_proxy_async_global();
+            chunk_bump_tile(p, prev_tm);
+        }
     } else if (warp >= 8) {
         // ------------------------------------------------------------ reduce (reducer units of this CTA)
         const int row = threadIdx.x - 256;
