@@ -269,7 +269,6 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
             // GEMM+RS pushes a running sum along the ranks (rank r adds its accumulator to rank
             // r-1's sum), so a tile's rank r+1 should run after its rank r: rank by rank over
             // blocks of tile pairs (each rank sweeps the block's tiles, as one GEMM would).
-            p->ring = 1;
             p->rank_group = 1;
             if (!p->chunk_ctr) {
                 // one block of all the tile pairs, raster groups of 8 pair rows: no padding, and

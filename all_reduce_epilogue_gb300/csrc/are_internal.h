@@ -125,7 +125,6 @@ struct GemmParams {
     int rot_cs;          // order chunks per owner segment
     int rot_ps;          // pair rows per owner segment
     int rot_w;           // tile columns per destination rotation (stripe)
-    int ring;            // CTA-pair kernel, GEMM+RS: push the running sum along the ranks
     uint32_t flags;
     int64_t debug_arg;
     uint64_t timeout_ns;

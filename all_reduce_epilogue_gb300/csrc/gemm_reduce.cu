@@ -659,9 +659,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 //               GEMM+AR stores bf16 partials (at R = 8 without its own row
 //               slice, which stays in shared memory);
 //   warps 8-11  reduce: GEMM+AR's two-shot all-reduce (every unit sums its row
-//               slice of the R partials in the order r = 0..R-1 and writes it
-//               to every view) and chunked GEMM+RS's gather at the tile's
-//               reducer, both fed by the loader warp.
+//               slice of the R partials in the order r = 0..R-1, fed by the
+//               loader warp, and writes it to every view); idle for GEMM+RS.
 // The drain never waits on a reduction (apart from GEMM+AR's bounded
 // own-slice wait, see the kernel), and the MMA never waits on the exchange.
 // ============================================================================
@@ -692,8 +691,8 @@ struct PUnit {
     int t;        // this CTA's 128x256 tile (row-major tile index)
     int tp;       // position of the tile pair in the unit order
     int j;        // position of the unit among its pair's R units (GEMM+AR: the row slice it reduces)
-    int tm, tn, r, own;
-    bool reducer, valid;
+    int tm, tn, r;
+    bool valid;
     bool pad;     // padding unit of the last rank block: skipped by every role
 };
 
@@ -703,8 +702,8 @@ struct PUnit {
 // run in groups of g: for the k-th group, every pair of the block runs its
 // units j = k*g .. k*g+g-1 (consecutively) before the next group starts.  g = 1
 // is rank by rank (a wave streams the operands of one or two ranks), g = R is
-// ranks innermost.  The reducer (j = R-1) stays last per pair.  Units past the
-// last pair (padding of the last block) are not valid.
+// ranks innermost.  Units past the last pair (padding of the last block) are
+// not valid.
 __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int u, int q) {
     PUnit U;
     int tp, j;
@@ -729,8 +728,7 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
     U.j = j;
     U.pad = tp >= num_pairs;
     if (U.pad) {  // padding unit: no tile
-        U.t = 0; U.tm = p.tiles_m; U.tn = 0; U.r = 0; U.own = 0;
-        U.reducer = false;
+        U.t = 0; U.tm = p.tiles_m; U.tn = 0; U.r = 0;
         U.valid = false;
         return U;
     }
@@ -761,26 +759,11 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
         tmp = first + in % gm;
         U.tn = in / gm;
     }
-    U.own = (mode == kModeRS) ? (tmp * 2 * kBM) / p.S : tp % p.R;
-    int r;
-    const bool ring = p.ring != 0;
-    if (p.rot_pc > 0 || mode == kModeAR || ring) {
-        // GEMM+RS on the push ring: rank r adds its accumulator to rank r-1's sum, so a tile's
-        // ranks run in the order 0..R-1 and each waits only for the unit before it.
-        // Rotated order (chunked GEMM+RS): a wave holds pairs of every owner segment, so every
-        // pair runs its ranks in the same order 0..R-1 (a wave then streams the operands of the
-        // same one or two ranks whatever the owners) and the owner's unit is not last.  Its
-        // reducer then waits for later units; they never wait on a reduction, so that wait
-        // ends too.  GEMM+AR: every unit reduces a row slice once all R units have published,
-        // so no unit has to come last either.
-        r = j;
-    } else {
-        // the owner's unit last, so its reducer finds the peers' partials already published
-        r = U.own + 1 + j;
-        while (r >= p.R) r -= p.R;
-    }
-    U.r = r;
-    U.reducer = !ring && (r == U.own);  // the push ring (GEMM+RS) has no gathering reducer
+    // A pair runs its ranks in the order 0..R-1: GEMM+RS pushes the running sum from rank to
+    // rank (rank r waits only for the same tile's rank r-1, an earlier unit), and each GEMM+AR
+    // unit reduces its row slice once all R units have published (later units never wait on
+    // a reduction, so that wait ends too).
+    U.r = j;
     U.tm = 2 * tmp + q;
     U.valid = U.tm < p.tiles_m;
     U.t = U.tm * p.tiles_n + U.tn;
@@ -877,7 +860,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
     const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row
-    const bool ring = (MODE == kModeRS) && p.ring != 0;
+    constexpr bool ring = (MODE == kModeRS);  // GEMM+RS pushes its running sum along the ranks
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
@@ -1071,9 +1054,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     if (!ok) break;
                     continue;
                 }
-                // GEMM+RS: the tile's reducer (its owner) loads all of it; GEMM+AR: every unit
-                // loads its row slice
-                if (!U.valid || (MODE == kModeRS && !U.reducer)) continue;
+                // GEMM+AR: every unit loads its row slice of the pair's R partials
+                if (!U.valid) continue;
                 bool ok = true;
                 uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
                 if (seen != full_mask) {
@@ -1100,36 +1082,22 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (!ok) break;
                 // generic-proxy acquire above, async-proxy (bulk copy) reads below
                 ptx::fence_proxy_async_global();
-                if (MODE == kModeAR) {
-                    // row slice U.j: groups of up to 16 rows; a stage holds one rank's group,
-                    // 1 KB per 64-byte column sub-tile (sub-tile st at st * 1 KB)
-                    const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
-                    for (int g0 = lo; g0 < hi && ok; g0 += 16) {
-                        const int nr = min(16, hi - g0);
-                        for (int r = 0; r < p.R; ++r) {
-                            if (own_slice && r == U.j) continue;  // on chip (sOwn)
-                            if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
-                            ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(2 * nsub * nr * 64));
-                            const uint8_t* src = pair_slot(p, U, r) + (size_t)g0 * 64;
-                            for (int st = 0; st < 2 * nsub; ++st)
-                                ptx::bulk_load(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
-                                               (uint32_t)(nr * 64), &pfull[ps]);
-                            issued |= 1u << ps;
-                            issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
-                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
-                        }
-                    }
-                } else {
-                    for (int j = 0; j < 2 * nsub && ok; ++j) {
-                        for (int r = 0; r < p.R; ++r) {
-                            if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
-                            ptx::mbar_arrive_expect_tx(&pfull[ps], kPSub2);
-                            const uint8_t* src = pair_slot(p, U, r) + (size_t)j * kPSub2;
-                            ptx::bulk_load(sP + ps * kPSub2, src, kPSub2, &pfull[ps]);
-                            issued |= 1u << ps;
-                            issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
-                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
-                        }
+                // row slice U.j: groups of up to 16 rows; a stage holds one rank's group,
+                // 1 KB per 64-byte column sub-tile (sub-tile st at st * 1 KB)
+                const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
+                for (int g0 = lo; g0 < hi && ok; g0 += 16) {
+                    const int nr = min(16, hi - g0);
+                    for (int r = 0; r < p.R; ++r) {
+                        if (own_slice && r == U.j) continue;  // on chip (sOwn)
+                        if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
+                        ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(2 * nsub * nr * 64));
+                        const uint8_t* src = pair_slot(p, U, r) + (size_t)g0 * 64;
+                        for (int st = 0; st < 2 * nsub; ++st)
+                            ptx::bulk_load(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
+                                           (uint32_t)(nr * 64), &pfull[ps]);
+                        issued |= 1u << ps;
+                        issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
                     }
                 }
                 if (!ok) break;
@@ -1276,7 +1244,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     }
                 }
                 ++nvalid;
-                if (MODE == kModeRS && ring && grp_bar_or<1>(bad)) { bad = true; break; }
+                if (ring && grp_bar_or<1>(bad)) { bad = true; break; }
                 if (MODE == kModeRS && ring_last) {
                     // the tile is complete: every earlier rank's bit was read by this unit's loader
                     // before it streamed S_(R-2), so the word can be re-armed now
@@ -1334,11 +1302,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             ptx::fence_proxy_async_global();
             chunk_bump_tile(p, prev_tm);
         }
-    } else if (warp >= 8) {
-        // ------------------------------------------------------------ reduce (reducer units of this CTA)
+    } else if (MODE == kModeAR && warp >= 8) {
+        // ------------------------------------------------------------ reduce (GEMM+AR's row slices)
         const int row = threadIdx.x - 256;
         const bool lead = (warp == 8);
-        int prev_tm = -1;  // chunk counting: the last reducer tile whose stores may still be in flight
         int nvalid = 0;    // GEMM+AR: valid units reduced (own-slice buffer nvalid & 1, as in the drain)
         int ps = 0;
         uint32_t pph = 0;
@@ -1470,94 +1437,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 ++nvalid;
                 continue;
             }
-            if (MODE == kModeAR || !U.reducer || !U.valid) continue;
-            const int row0 = U.tm * kBM;
-            for (int c = 0; c < kBN / 64; ++c) {  // 64-column output chunks
-                uint32_t outw[32];
-                {
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {  // partial sub-tile 4c + h: columns 16h..16h+15 of the chunk
-                        float acc[16];
-                        for (int qq = 0; qq < p.R; ++qq) {
-                            uint32_t v[16];
-                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
-                            read_row_sw64(sP + ps * kPSub2, row, v);
-                            ptx::mbar_arrive(&pempty[ps]);
-                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
-                            if (qq == 0) {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) acc[e] = __uint_as_float(v[e]);
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) acc[e] = acc[e] + __uint_as_float(v[e]);
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) outw[8 * h + e] = pack_bf16x2(acc[2 * e], acc[2 * e + 1]);
-                    }
-                }
-                const int sb = 0;  // one staging buffer: lane 0 issues and waits for its stores
-                if (lead && lane == 0) ptx::bulk_wait_read0();
-                if (grp_bar_or<2>(bad)) { bad = true; break; }
-                write_row_sw128(sOut, row, outw);
-                ptx::fence_proxy_async_shared();
-                grp_bar<2>();
-                if (lead && lane == 0) {
-                    const int x = U.tn * kBN + c * 64;
-                    if (x < p.N) {
-                        // owner-boundary flush: one store per (segment piece, H-row box)
-                        const int row_end = min(row0 + kBM, p.M);
-                        for (int r0 = row0; r0 < row_end;) {
-                            const int s = r0 / p.S;
-                            const int e = min((s + 1) * p.S, row_end);
-                            for (int rb = r0; rb < e; rb += p.H)
-                                ptx::tma_store_2d(&p.tmOut[s], sOut + sb * kSubBytes + (rb - row0) * 128, x,
-                                                  rb - s * p.S);
-                            r0 = e;
-                        }
-                        ptx::bulk_commit();
-                    }
-                }
-            }
-            if (bad) break;
-            if (lead && lane == 0) {
-                if (MODE == kModeRS && (p.flags & ARE_DEBUG_LOG_PIECES)) {
-                    int32_t* log = p.pieces + (size_t)U.t * kPieceWords;
-                    const int row_end = min(row0 + kBM, p.M);
-                    int n = 0;
-                    for (int r0 = row0; r0 < row_end && n < (kPieceWords - 3) / 3;) {
-                        const int s = r0 / p.S;
-                        const int e = min((s + 1) * p.S, row_end);
-                        log[3 + 3 * n] = s; log[4 + 3 * n] = r0; log[5 + 3 * n] = e;
-                        ++n;
-                        r0 = e;
-                    }
-                    log[0] = U.tm; log[1] = U.tn; log[2] = n;
-                }
-                // re-arm the tile's mask word for the next call
-                if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
-                if (MODE == kModeRS && p.chunk_ctr) {
-                    // count the previous reducer tile's pieces once its stores have completed
-                    // (all but this tile's bulk groups); this tile's are counted after the next
-                    if (prev_tm >= 0) {
-                        const int rem_cols = p.N - U.tn * kBN;
-                        ptx::bulk_wait_upto(min(kBN / 64, (rem_cols + 63) / 64));
-                        ptx::fence_proxy_async_global();
-                        chunk_bump_tile(p, prev_tm);
-                    }
-                    prev_tm = U.tm;
-                }
-            }
         }
         if (bad) *abort_flag = 1u;
         if (lead && lane == 0) prof_add(p, 7, w_pfull);
-        if (lead && lane == 0) {
-            ptx::bulk_wait0();
-            if (MODE == kModeRS && p.chunk_ctr && prev_tm >= 0 && !bad) {
-                ptx::fence_proxy_async_global();
-                chunk_bump_tile(p, prev_tm);
-            }
-        }
+        if (lead && lane == 0) ptx::bulk_wait0();
     }
 
     __syncwarp();

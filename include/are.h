@@ -290,10 +290,11 @@ ARE_API are_status are_workspace_set_gemm_order(are_ws* ws, int group_m, int blo
  * owner segments: chunk c of segment s is a band of the 128-row output tiles
  * that intersect s (their count n_s split into C_s = `chunks` halved until it
  * divides n_s), and it completes once every 128x256 tile of the band has been
- * reduced and its rows stored into segment s.  The elected reducer publishes
- * the chunk's generation (how many calls have completed it since the
- * workspace was created or reset) to host-mapped memory, where
- * are_chunk_wait() sees it while the kernel is still running.
+ * reduced and its rows stored into segment s.  The unit whose piece completes
+ * the chunk (elected by the counters) publishes the chunk's generation (how
+ * many calls have completed it since the workspace was created or reset) to
+ * host-mapped memory, where are_chunk_wait() sees it while the kernel is
+ * still running.
  *  chunks : chunks per owner segment, 0 (off, the default) .. 64.
  *  stripe : the CTA-pair kernel's tile order while chunking is on, where the
  *           owner segments are whole 256-row tile pairs (M/R % 256 == 0):
@@ -316,7 +317,7 @@ ARE_API are_status are_chunk_generation(are_ws* ws, uint64_t* generation);
 
 /* Host-side wait for chunk `chunk` of owner segment `segment` to reach
  * `generation` (compared modulo 2^32): polls the host-mapped word that the
- * elected reducer of the chunk writes, so it returns while the GEMM+RS kernel
+ * unit completing the chunk writes, so it returns while the GEMM+RS kernel
  * is still running, as soon as that chunk's rows are in device memory.  No
  * GPU-side waiter is involved.  Returns ARE_OK, ARE_ETIMEOUT after
  * `timeout_ns`, ARE_EINVAL for an index outside the workspace. */
