@@ -1086,8 +1086,10 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 // generic-proxy acquire above, async-proxy (bulk copy) reads below
                 ptx::fence_proxy_async_global();
                 // row slice U.j: groups of up to 16 rows; a stage holds one rank's group,
-                // 1 KB per 64-byte column sub-tile (sub-tile st at st * 1 KB)
+                // 1 KB per 64-byte column sub-tile (sub-tile st at st * 1 KB); each slice of a
+                // partial is read once, so evict-first
                 const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
+                const uint64_t pol_p = ptx::policy_evict_first();
                 for (int g0 = lo; g0 < hi && ok; g0 += 16) {
                     const int nr = min(16, hi - g0);
                     for (int r = 0; r < p.R; ++r) {
@@ -1096,8 +1098,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                         ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(2 * nsub * nr * 64));
                         const uint8_t* src = pair_slot(p, U, r) + (size_t)g0 * 64;
                         for (int st = 0; st < 2 * nsub; ++st)
-                            ptx::bulk_load(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
-                                           (uint32_t)(nr * 64), &pfull[ps]);
+                            ptx::bulk_load_hint(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
+                                                (uint32_t)(nr * 64), &pfull[ps], pol_p);
                         issued |= 1u << ps;
                         issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
                         if (++ps == kPStages2) { ps = 0; pph ^= 1u; }

@@ -60,8 +60,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # line reports null.
 KERNEL_SOURCES = {"gemm_rs": "gemm_reduce.cu", "gemm_ar": "gemm_reduce.cu", "allreduce_rmsnorm": "ar_rmsnorm.cu"}
 NCU_TRAFFIC = {
-    "gemm_rs": (6773.6e6, "fa1d9a3612e9dfb7"),
-    "gemm_ar": (2819.1e6, "fa1d9a3612e9dfb7"),
+    "gemm_rs": (6674.8e6, "5a92ad4d79000dbb"),
+    "gemm_ar": (2769.3e6, "5a92ad4d79000dbb"),
     "allreduce_rmsnorm": (626.4e6, "a4af1f7bd1f46c00"),
 }
 
