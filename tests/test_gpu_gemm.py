@@ -183,6 +183,36 @@ def test_unpublished_tile_times_out_and_reset_recovers(oracle, single_cta):
     check_close(got, oracle.gemm_rs(A, B), "after reset")
 
 
+def test_ring_rank_unpublished_mid_chain_times_out(oracle):
+    """GEMM+RS on the CTA-pair kernel's push ring, broken in the middle of a
+    tile's chain: rank 2 of the first tile pair adds S_1 and stores S_2 but never
+    sets its ready bit, so rank 3's loader times out waiting for it; every CTA
+    returns with a timeout status naming one of the pair's tiles, and a reset
+    recovers.  The ranks run one after the other over a single block of all
+    tile pairs, so the unit of rank r and tile pair p is r * pairs + p
+    (here 2 pairs: unit 4)."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    R, M, N, K = 4, 256, 512, 128
+    A, B = synth.gemm_inputs(R, M, N, K, 23)
+    dA, dB = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    with make_ws(timeout_ns=20_000_000) as ws:
+        ws.set_debug(are.DEBUG_PAIR_CTA | are.DEBUG_SKIP_PUBLISH, 4)
+        are.gemm_rs(dA, dB, out, ws)
+        st = ws.device_status()
+        assert ws.last_launch()["kernel"] == "gemm_pair_kernel"
+        assert st["status"] == are.ETIMEOUT and st["code"] in (are.DEV_MASK_TIMEOUT, are.DEV_PIPE_TIMEOUT), st
+        if st["code"] == are.DEV_MASK_TIMEOUT:
+            assert st["a"] in (0, N // 256), st
+        ws.set_debug(are.DEBUG_PAIR_CTA)
+        ws.reset()
+        got = host_f32(run_rs(ws, A, B))
+    check_close(got, oracle.gemm_rs(A, B), "after reset")
+
+
 def test_gemm_ar_unpublished_unit_times_out_with_own_slice(oracle):
     """GEMM+AR at R = 8 through the CTA-pair kernel, where each unit keeps its
     own row slice on chip and a drain waits for the reduction two units back:
