@@ -30,6 +30,7 @@ OP_GEMM_RS, OP_GEMM_AR, OP_ALLREDUCE_RMSNORM = 1, 2, 3
 # debug flags
 DEBUG_NO_REARM, DEBUG_LOG_PIECES, DEBUG_COUNT_CANON, DEBUG_SKIP_PUBLISH, DEBUG_SKIP_STAGE = 1, 2, 4, 8, 16
 DEBUG_SINGLE_CTA, DEBUG_WAIT_PROFILE, DEBUG_AR_ONESHOT, DEBUG_AR_LAMPORT, DEBUG_PAIR_CTA = 32, 64, 128, 256, 512
+DEBUG_RS_RING, DEBUG_RS_SPLIT = 1024, 2048
 # device status codes
 DEV_OK, DEV_MASK_TIMEOUT, DEV_STAGE_TIMEOUT, DEV_PIPE_TIMEOUT = 0, 1, 2, 3
 # snapshot kinds

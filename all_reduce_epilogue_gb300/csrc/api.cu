@@ -197,8 +197,6 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     for (int r = 0; r < R && e == cudaSuccess; ++r) {
         e = make_tmap_bf16(&p->tmA[r], A[r], (uint64_t)K, (uint64_t)M, kBK, kBM);
         if (e == cudaSuccess) e = make_tmap_bf16(&p->tmB[r], B[r], (uint64_t)N, (uint64_t)K, 64, kBK);
-        if (e == cudaSuccess && mode == kModeRS)
-            e = make_tmap_bf16(&p->tmOut[r], out[r], (uint64_t)N, (uint64_t)S, 64, (uint32_t)H);
     }
     // CTA pairs (256-row tiles) wherever there are at least two tile rows and
     // the device can co-schedule the clusters; one CTA per tile otherwise.  GEMM+AR
@@ -207,12 +205,33 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     // B, and the pair kernel spreads the reduction over a pair's R units and keeps every
     // SM streaming (R=8, M=64, N=7168, K=2048: 58.6 against 64.5 us).
     const int clusters = ws->pair_clusters;
-    // Below one wave of pairs the reduce of the last (only) wave is the kernel's tail, and
-    // the one-CTA kernel's deeper partial buffer (and its reducer's own partial kept in
-    // TMEM) finishes it sooner: R=4, M=256 measured 33 us against 69 us.
     const int64_t pair_units = (int64_t)((tiles_m + 1) / 2) * tiles_n * R;
     const bool pair_ok = (tiles_m >= 2 || mode == kModeAR) && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
-    const bool use_pair = pair_ok && (pair_units > clusters || (ws->debug_flags & ARE_DEBUG_PAIR_CTA));
+    // GEMM+RS on the pair kernel: the running sum pushed along the ranks, or every unit of a tile
+    // reducing its row slice (two-shot, as GEMM+AR).  The ring's R drains of a tile run one after
+    // the other, which a problem of many waves hides and one of a few waves does not.  Measured
+    // (us per call, ring / split / one-CTA kernel; waves of pair units): R=4, N=4096, K=2048 at
+    // M=256 42.7 / 33.6 / 35.4 (0.8), M=512 52.4 / 46.1 / 54.1 (1.7), M=1024 62.1 / 68.1 / 89.9
+    // (3.4), M=4096 172.7 / 199.0 / 239.1; R=8, N=7168, K=2048, M=256 97.5 / 75.4 / 118.4 (2.9);
+    // R=8, N=8192, K=4096, M=512 174.7 / 198.2 / 268.4 (6.7); R=2, N=4096, K=2048, M=256
+    // 26.3 / 30.0 / 29.1 (0.4: a chain of two).  So: the split for R >= 4 up to three waves, the
+    // ring otherwise, and the pair kernel (either way) rather than the one-CTA kernel from two
+    // tile rows on.  Chunked calls count a tile's pieces at the ring's last rank: always the ring.
+    bool rs_split = mode == kModeRS && ws->chunks == 0 && R >= 4 && pair_units <= 3 * (int64_t)clusters;
+    if (ws->debug_flags & ARE_DEBUG_RS_SPLIT) rs_split = mode == kModeRS && ws->chunks == 0;
+    if (ws->debug_flags & ARE_DEBUG_RS_RING) rs_split = false;
+    // GEMM+AR below one wave of pairs: the one-CTA kernel (the pair kernel from one wave on, or
+    // with a single tile row, see above)
+    const bool use_pair = pair_ok && (pair_units > clusters || mode == kModeRS || (ws->debug_flags & ARE_DEBUG_PAIR_CTA));
+    if (mode == kModeRS) {
+        // owner-segment maps: H-row boxes for the ring's and the one-CTA kernel's piece stores,
+        // 16-row boxes (where segments are whole 16-row groups) for the row slices' groups
+        if (use_pair && rs_split && H > 16) H = 16;
+        for (int r = 0; r < R && e == cudaSuccess; ++r) {
+            e = make_tmap_bf16(&p->tmOut[r], out[r], (uint64_t)N, (uint64_t)S, 64, (uint32_t)H);
+            p->views[r] = out[r];
+        }
+    }
     // GEMM+AR views: the one-CTA kernel stores whole 128-row tiles, the pair kernel 16-row
     // groups of a unit's row slice (boxes of 64 columns either way)
     for (int v = 0; v < nviews && e == cudaSuccess; ++v) {
@@ -265,7 +284,11 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
             p->rot_pc = ps / cs;
             p->rot_w = ws->chunk_stripe > 0 ? std::min<int>(ws->chunk_stripe, (int)tiles_n) : (int)tiles_n;
         }
-        if (mode == kModeRS) {
+        if (mode == kModeRS && rs_split) {
+            // two-shot, as GEMM+AR: a pair's R units consecutive
+            p->rs_split = 1;
+            p->rank_group = 1;
+        } else if (mode == kModeRS) {
             // GEMM+RS pushes a running sum along the ranks (rank r adds its accumulator to rank
             // r-1's sum), so a tile's rank r+1 should run after its rank r: rank by rank over
             // blocks of tile pairs (each rank sweeps the block's tiles, as one GEMM would).
@@ -305,7 +328,8 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
             p->num_pair_units = (int)(blocks * p->block_tiles * R);
         }
         const int grid = 2 * (int)std::min<int64_t>(p->num_pair_units, clusters);
-        ws->last = are_launch_info{ARE_KERNEL_GEMM_PAIR, grid, gemm_pair_threads(), 2, p->block_tiles, 0,
+        ws->last = are_launch_info{ARE_KERNEL_GEMM_PAIR, grid, gemm_pair_threads(), 2, p->block_tiles,
+                                   (mode == kModeAR || p->rs_split) ? 1 : 0,
                                    p->block_tiles > 0 ? p->rank_group : R, p->group_m};
         e = launch_gemm_pair(*p, mode, grid, s);
     } else {

@@ -99,7 +99,8 @@ struct GemmParams {
     CUtensorMap tmB[kMaxRanks];
     CUtensorMap tmOut[kMaxRanks];  // GEMM+RS: owner segments (64 x H boxes); GEMM+AR: the distinct views
                                    // (64 x 128 boxes for the one-CTA kernel, 64 x 16 for the pair kernel)
-    are_bf16* views[kMaxRanks];  // GEMM+AR: distinct output views (ragged row groups: st.global)
+    are_bf16* views[kMaxRanks];  // GEMM+AR: distinct output views; GEMM+RS with rs_split: the owner
+                                 // segments (row groups that no box covers: st.global)
     uint8_t* part;       // [R][T][tile part bytes]
     uint32_t* mask;      // [T]
     DevStatus* status;
@@ -113,6 +114,8 @@ struct GemmParams {
     int tiles_m, tiles_n, num_tiles, num_units, num_kb;
     int pairs_m, num_pair_units;  // CTA-pair kernel: 256-row tile pairs, R units per pair
     int block_tiles;     // CTA-pair kernel: tile pairs per rank block (0 = ranks innermost)
+    int rs_split;        // CTA-pair kernel, GEMM+RS: 1 = every unit reduces its row slice of the tile
+                         // (two-shot, as GEMM+AR); 0 = the running sum is pushed along the ranks
     int rank_group;      // CTA-pair kernel: ranks run together inside a block (1 = rank by rank)
     uint32_t* cons;      // CTA-pair kernel, GEMM+AR: row-slice readers done per tile (0 between calls)
     int group_m;         // tile raster: rows of tiles (pairs) per group

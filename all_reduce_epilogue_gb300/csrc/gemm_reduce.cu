@@ -656,11 +656,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) gemm_reduce_kernel(const __gr
 //               first adds S_(r-1) (fed by the loader warp into the 3-stage
 //               partial buffer once bit r-1 is set) and stores S_r; the last
 //               rank rounds to bf16 and stores the owner pieces with TMA.
-//               GEMM+AR stores bf16 partials (at R = 8 without its own row
-//               slice, which stays in shared memory);
-//   warps 8-11  reduce: GEMM+AR's two-shot all-reduce (every unit sums its row
-//               slice of the R partials in the order r = 0..R-1, fed by the
-//               loader warp, and writes it to every view); idle for GEMM+RS.
+//               Problems of a few waves, where that chain of drains would be
+//               the tail, split the reduction instead (rs_split): every unit
+//               stores its fp32 partial, as GEMM+AR does its bf16 partial (at
+//               R = 8 without its own row slice, which stays in shared memory);
+//   warps 8-11  reduce, two-shot (GEMM+AR, and GEMM+RS with rs_split): every
+//               unit sums its row slice of the tile's R partials in the order
+//               r = 0..R-1, fed by the loader warp, and writes it to every view
+//               (GEMM+AR) or to the rows' owner segments (GEMM+RS).
 // The drain never waits on a reduction (apart from GEMM+AR's bounded
 // own-slice wait, see the kernel), and the MMA never waits on the exchange.
 // ============================================================================
@@ -759,10 +762,10 @@ __device__ __forceinline__ PUnit decode_pair(const GemmParams& p, int mode, int 
         tmp = first + in % gm;
         U.tn = in / gm;
     }
-    // A pair runs its ranks in the order 0..R-1: GEMM+RS pushes the running sum from rank to
-    // rank (rank r waits only for the same tile's rank r-1, an earlier unit), and each GEMM+AR
-    // unit reduces its row slice once all R units have published (later units never wait on
-    // a reduction, so that wait ends too).
+    // A pair runs its ranks in the order 0..R-1: GEMM+RS on the ring pushes the running sum
+    // from rank to rank (rank r waits only for the same tile's rank r-1, an earlier unit), and
+    // a two-shot unit (GEMM+AR, GEMM+RS with rs_split) reduces its row slice once all R units
+    // have published (later units never wait on a reduction, so that wait ends too).
     U.r = j;
     U.tm = 2 * tmp + q;
     U.valid = U.tm < p.tiles_m;
@@ -860,7 +863,13 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
     const int cl = blockIdx.x >> 1;
     const int G2 = gridDim.x >> 1;
     const int nsub = (MODE == kModeRS) ? 8 : 4;  // 128-byte column chunks of a partial row
-    constexpr bool ring = (MODE == kModeRS);  // GEMM+RS pushes its running sum along the ranks
+    // GEMM+RS pushes its running sum along the ranks, or (rs_split) reduces like GEMM+AR: every
+    // unit sums its row slice of the tile's R partials (two-shot)
+    const bool ring = (MODE == kModeRS) && !p.rs_split;
+    const bool split = !ring;
+    // a 16-row group of a row slice is loaded as stages of 8 partial sub-tiles (8 KB): one for
+    // GEMM+AR's bf16 partial rows (512 bytes), two for GEMM+RS's fp32 rows (1 KB)
+    constexpr int kHalves = (MODE == kModeRS) ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages2; ++s) { ptx::mbar_init(&full[s], 1); ptx::mbar_init(&empty[s], 1); }
@@ -1057,7 +1066,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     if (!ok) break;
                     continue;
                 }
-                // GEMM+AR: every unit loads its row slice of the pair's R partials
+                // two-shot: every unit loads its row slice of the pair's R partials
                 if (!U.valid) continue;
                 bool ok = true;
                 uint32_t seen = ptx::ld_acquire_gpu(&p.mask[U.t]);
@@ -1085,24 +1094,26 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 if (!ok) break;
                 // generic-proxy acquire above, async-proxy (bulk copy) reads below
                 ptx::fence_proxy_async_global();
-                // row slice U.j: groups of up to 16 rows; a stage holds one rank's group,
-                // 1 KB per 64-byte column sub-tile (sub-tile st at st * 1 KB); each slice of a
-                // partial is read once, so evict-first
+                // row slice U.j: groups of up to 16 rows; a stage holds one rank's group of 8
+                // sub-tiles, 1 KB per 64-byte column sub-tile (sub-tile hf * 8 + st at st * 1 KB of
+                // the group's stage hf); each slice of a partial is read once, so evict-first
                 const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
                 const uint64_t pol_p = ptx::policy_evict_first();
                 for (int g0 = lo; g0 < hi && ok; g0 += 16) {
                     const int nr = min(16, hi - g0);
-                    for (int r = 0; r < p.R; ++r) {
-                        if (own_slice && r == U.j) continue;  // on chip (sOwn)
-                        if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
-                        ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(2 * nsub * nr * 64));
-                        const uint8_t* src = pair_slot(p, U, r) + (size_t)g0 * 64;
-                        for (int st = 0; st < 2 * nsub; ++st)
-                            ptx::bulk_load_hint(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
-                                                (uint32_t)(nr * 64), &pfull[ps], pol_p);
-                        issued |= 1u << ps;
-                        issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
-                        if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                    for (int hf = 0; hf < kHalves && ok; ++hf) {
+                        for (int r = 0; r < p.R; ++r) {
+                            if (own_slice && r == U.j) continue;  // on chip (sOwn)
+                            if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
+                            ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(8 * nr * 64));
+                            const uint8_t* src = pair_slot(p, U, r) + (size_t)(hf * 8) * kPSub2 + (size_t)g0 * 64;
+                            for (int st = 0; st < 8; ++st)
+                                ptx::bulk_load_hint(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
+                                                    (uint32_t)(nr * 64), &pfull[ps], pol_p);
+                            issued |= 1u << ps;
+                            issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
+                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
+                        }
                     }
                 }
                 if (!ok) break;
@@ -1307,8 +1318,8 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             ptx::fence_proxy_async_global();
             chunk_bump_tile(p, prev_tm);
         }
-    } else if (MODE == kModeAR && warp >= 8) {
-        // ------------------------------------------------------------ reduce (GEMM+AR's row slices)
+    } else if (warp >= 8 && split) {
+        // ------------------------------------------------------------ reduce (two-shot row slices)
         const int row = threadIdx.x - 256;
         const bool lead = (warp == 8);
         int nvalid = 0;    // GEMM+AR: valid units reduced (own-slice buffer nvalid & 1, as in the drain)
@@ -1321,10 +1332,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
             const int u = i * G2 + (cl + i) % G2;
             if (u >= p.num_pair_units) continue;
             const PUnit U = decode_pair(p, MODE, u, (int)q);
-            if (MODE == kModeAR && !U.pad && U.valid) {
-                // ---- GEMM+AR: this unit reduces row slice U.j of its tile (a two-shot all-reduce:
-                // rank j sums slice j of all R partials in the order r = 0..R-1, then writes it
-                // to every view), so every unit of a pair takes 1/R of the tile's reduction
+            if (!U.pad && U.valid) {
+                // ---- this unit reduces row slice U.j of its tile (two-shot: rank j sums slice j of
+                // all R partials in the order r = 0..R-1, then writes it to every view, GEMM+AR, or
+                // to its owner segments, GEMM+RS), so every unit of a pair takes 1/R of the tile's
+                // reduction
                 const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
                 const int st = row >> 4, rr = row & 15;  // 64-byte column sub-tile, row in the group
                 const int wq = warp - 8;
@@ -1333,100 +1345,129 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 for (int g0 = lo; g0 < hi; g0 += 16) {
                     const int nr = min(16, hi - g0);
                     const int trow = g0 + rr;  // tile row of this thread
+                    // GEMM+AR: 32 bf16 columns of sub-tile st; GEMM+RS: 16 fp32 columns of sub-tiles
+                    // st (acc[0..15]) and 8 + st (acc[16..31])
                     float acc[32];
-                    for (int qq = 0; qq < p.R; ++qq) {
-                        const bool mine = own_slice && qq == U.j;
-                        // The own slice was written by this CTA's drain before it published the unit's
-                        // mask bit; the loader acquired the full mask before filling this unit's stages,
-                        // so a wait on one of them orders those writes first.  For rank 0 that is the
-                        // wait on the next stage (rank 1's, not consumed here); for a later rank the
-                        // waits on the stages before it already did.
-                        if (!mine || qq == 0)
-                            if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
-                        uint32_t v[16];
-                        if (rr < nr) {
-                            const uint8_t* rp = (mine ? own_buf : sP + ps * kPSub2) + st * 1024 + rr * 64;
+                    for (int hf = 0; hf < kHalves; ++hf) {
+                        for (int qq = 0; qq < p.R; ++qq) {
+                            const bool mine = own_slice && qq == U.j;
+                            // The own slice was written by this CTA's drain before it published the unit's
+                            // mask bit; the loader acquired the full mask before filling this unit's stages,
+                            // so a wait on one of them orders those writes first.  For rank 0 that is the
+                            // wait on the next stage (rank 1's, not consumed here); for a later rank the
+                            // waits on the stages before it already did.
+                            if (!mine || qq == 0)
+                                if (!wait_bar_prof(&pfull[ps], pph, abort_flag, p, 15, u, w_pfull, 200)) bad = true;
+                            uint32_t v[16];
+                            if (rr < nr) {
+                                const uint8_t* rp = (mine ? own_buf : sP + ps * kPSub2) + st * 1024 + rr * 64;
 #pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                const uint4 x = *reinterpret_cast<const uint4*>(rp + ((c ^ ((trow >> 1) & 3)) << 4));
-                                v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+                                for (int c = 0; c < 4; ++c) {
+                                    const uint4 x = *reinterpret_cast<const uint4*>(rp + ((c ^ ((trow >> 1) & 3)) << 4));
+                                    v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) v[e] = 0u;
                             }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] = 0u;
-                        }
-                        if (!mine) {
-                            ptx::mbar_arrive(&pempty[ps]);
-                            if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
-                        }
-                        if (qq == 0) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                acc[2 * e] = __uint_as_float(v[e] << 16);
-                                acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+                            if (!mine) {
+                                ptx::mbar_arrive(&pempty[ps]);
+                                if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
                             }
-                        } else {
+                            if (MODE == kModeRS) {
+                                float* a = acc + 16 * hf;
+                                if (qq == 0) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
-                                acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
+                                    for (int e = 0; e < 16; ++e) a[e] = __uint_as_float(v[e]);
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) a[e] = a[e] + __uint_as_float(v[e]);
+                                }
+                            } else if (qq == 0) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    acc[2 * e] = __uint_as_float(v[e] << 16);
+                                    acc[2 * e + 1] = __uint_as_float(v[e] & 0xFFFF0000u);
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    acc[2 * e] = acc[2 * e] + __uint_as_float(v[e] << 16);
+                                    acc[2 * e + 1] = acc[2 * e + 1] + __uint_as_float(v[e] & 0xFFFF0000u);
+                                }
                             }
                         }
                     }
-                    // A full group of 16 rows is staged as four 128B-swizzled boxes of 64 columns
-                    // (16 rows x 128 bytes each) and written to every view by TMA tensor stores,
-                    // one box per view and 64 columns.  A ragged group (R not dividing 128) is
-                    // staged as 16 x 512-byte rows (16-byte chunk k of row rr at position k ^ rr)
-                    // and written with whole-row 16-byte stores, so no box covers rows of
-                    // another unit's slice.  The issuing thread waits until the previous group's
-                    // stores have read the staging buffer; the barrier then orders the rewrite.
-                    const bool tma_views = (nr == 16);
+                    // The group's 16 rows x 256 bf16 columns (512 bytes a row) leave in 16-byte chunks:
+                    // this thread holds four, acc[8n..8n+7] for n = 0..3, at chunk k(n) of its row.
+                    // A full group (16 rows, aligned to an owner segment for GEMM+RS) is staged as four
+                    // 128B-swizzled boxes of 64 columns (16 rows x 128 bytes each) and written by TMA
+                    // tensor stores, one box per view (GEMM+AR) or into the rows' owner segment (GEMM+RS)
+                    // and 64 columns.  Any other group is staged as 16 x 512-byte rows (16-byte chunk k of
+                    // row rr at position k ^ rr) and written with whole-row 16-byte stores, so no box
+                    // covers rows of another unit's slice or another segment.  The issuing thread waits
+                    // until the previous group's stores have read the staging buffer; the barrier then
+                    // orders the rewrite.
+                    const int y = U.tm * kBM + g0;
+                    const bool tma_out = (nr == 16) && (MODE == kModeAR || (p.H == 16 && (g0 & 15) == 0));
                     if (lead && lane == 0) ptx::bulk_wait_read0();
                     if (grp_bar_or<2>(bad)) { bad = true; break; }
                     // every read of the own slice is done: hand its buffer back to the drain
                     if (own_slice && lead && lane == 0) ptx::mbar_arrive(&ownfree[oslot]);
-                    if (tma_views) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const int k = st * 4 + c;  // 16-byte chunk of the 512-byte row
-                            *reinterpret_cast<uint4*>(sOut + (k >> 3) * 2048 + rr * 128 + (((k & 7) ^ (rr & 7)) << 4)) =
-                                make_uint4(pack_bf16x2(acc[8 * c], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
-                                           pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]),
-                                           pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
-                        }
+                    for (int n = 0; n < 4; ++n) {
+                        const int k = (MODE == kModeRS) ? ((n >> 1) * 16 + st * 2 + (n & 1)) : (st * 4 + n);
+                        uint8_t* dst = tma_out ? sOut + (k >> 3) * 2048 + rr * 128 + (((k & 7) ^ (rr & 7)) << 4)
+                                               : sOut + rr * 512 + ((k ^ rr) << 4);
+                        *reinterpret_cast<uint4*>(dst) =
+                            make_uint4(pack_bf16x2(acc[8 * n], acc[8 * n + 1]), pack_bf16x2(acc[8 * n + 2], acc[8 * n + 3]),
+                                       pack_bf16x2(acc[8 * n + 4], acc[8 * n + 5]),
+                                       pack_bf16x2(acc[8 * n + 6], acc[8 * n + 7]));
+                    }
+                    if (tma_out) {
                         ptx::fence_proxy_async_shared();
                         grp_bar<2>();
                         if (lead && lane == 0) {
-                            // the views are read by nothing in this kernel: evict-first keeps the
+                            // the outputs are read by nothing in this kernel: evict-first keeps the
                             // operand panels and partials in L2 (648 -> 645 us alone at R=8,
                             // M=4096, N=7168, K=2048)
                             const uint64_t pol_v = ptx::policy_evict_first();
-                            const int y = U.tm * kBM + g0;
-                            for (int w = 0; w < p.nviews; ++w)
+                            if (MODE == kModeRS) {
+                                const int sg = y / p.S;  // the group lies inside one owner segment
+                                if (y < p.M) {
 #pragma unroll
-                                for (int b = 0; b < 4; ++b)  // boxes past N or M would store nothing
-                                    if (U.tn * kBN + b * 64 < p.N && y < p.M)
-                                        ptx::tma_store_2d_hint(&p.tmOut[w], sOut + b * 2048, U.tn * kBN + b * 64, y, pol_v);
+                                    for (int b = 0; b < 4; ++b)  // boxes past N would store nothing
+                                        if (U.tn * kBN + b * 64 < p.N)
+                                            ptx::tma_store_2d_hint(&p.tmOut[sg], sOut + b * 2048, U.tn * kBN + b * 64,
+                                                                   y - sg * p.S, pol_v);
+                                }
+                            } else {
+                                for (int w = 0; w < p.nviews; ++w)
+#pragma unroll
+                                    for (int b = 0; b < 4; ++b)  // boxes past N or M would store nothing
+                                        if (U.tn * kBN + b * 64 < p.N && y < p.M)
+                                            ptx::tma_store_2d_hint(&p.tmOut[w], sOut + b * 2048, U.tn * kBN + b * 64, y,
+                                                                   pol_v);
+                            }
                             ptx::bulk_commit();
                         }
                         continue;
                     }
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4*>(sOut + rr * 512 + (((st * 4 + c) ^ rr) << 4)) =
-                            make_uint4(pack_bf16x2(acc[8 * c], acc[8 * c + 1]), pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3]),
-                                       pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5]),
-                                       pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]));
                     grp_bar<2>();
                     const int gcol = U.tn * kBN + lane * 8;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int orr = wq + 4 * i;
-                        const int grow = U.tm * kBM + g0 + orr;
+                    for (int i2 = 0; i2 < 4; ++i2) {
+                        const int orr = wq + 4 * i2;
+                        const int grow = y + orr;
                         if (orr < nr && grow < p.M && gcol < p.N) {
                             const uint4 val = *reinterpret_cast<const uint4*>(sOut + orr * 512 + ((lane ^ orr) << 4));
-                            for (int w = 0; w < p.nviews; ++w)
-                                ptx::st_stream_v4(p.views[w] + (size_t)grow * p.N + gcol, val);
+                            if (MODE == kModeRS) {
+                                const int sg = grow / p.S;
+                                ptx::st_stream_v4(p.views[sg] + (size_t)(grow - sg * p.S) * p.N + gcol, val);
+                            } else {
+                                for (int w = 0; w < p.nviews; ++w)
+                                    ptx::st_stream_v4(p.views[w] + (size_t)grow * p.N + gcol, val);
+                            }
                         }
                     }
                 }
@@ -1436,11 +1477,25 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     const uint32_t old = atomicAdd(&p.cons[U.t], 1u);
                     if (old == (uint32_t)p.R - 1u) {
                         atomicExch(&p.cons[U.t], 0u);
+                        if (MODE == kModeRS && (p.flags & ARE_DEBUG_LOG_PIECES)) {
+                            // the tile's owner pieces (its R slices were stored by its R units)
+                            int32_t* log = p.pieces + (size_t)U.t * kPieceWords;
+                            const int row0 = U.tm * kBM;
+                            const int row_end = min(row0 + kBM, p.M);
+                            int n = 0;
+                            for (int r0 = row0; r0 < row_end && n < (kPieceWords - 3) / 3;) {
+                                const int sg = r0 / p.S;
+                                const int e = min((sg + 1) * p.S, row_end);
+                                log[3 + 3 * n] = sg; log[4 + 3 * n] = r0; log[5 + 3 * n] = e;
+                                ++n;
+                                r0 = e;
+                            }
+                            log[0] = U.tm; log[1] = U.tn; log[2] = n;
+                        }
                         if (!(p.flags & ARE_DEBUG_NO_REARM)) atomicExch(&p.mask[U.t], 0u);
                     }
                 }
                 ++nvalid;
-                continue;
             }
         }
         if (bad) *abort_flag = 1u;

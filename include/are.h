@@ -124,8 +124,12 @@ enum {
                                      to the counters (see ARE_SNAP_COUNTERS) */
     ARE_DEBUG_AR_ONESHOT = 128u,  /* AR+RMSNorm: take the one-shot path whatever the size (where a row fits) */
     ARE_DEBUG_AR_LAMPORT = 256u,  /* AR+RMSNorm: take the Lamport path whatever the size */
-    ARE_DEBUG_PAIR_CTA = 512u     /* GEMM: use the CTA-pair kernel wherever it applies (two or more tile rows;
+    ARE_DEBUG_PAIR_CTA = 512u,    /* GEMM: use the CTA-pair kernel wherever it applies (two or more tile rows;
                                      GEMM+AR also one), also below one wave of pairs */
+    ARE_DEBUG_RS_RING = 1024u,    /* GEMM+RS on the CTA-pair kernel: push the running sum along the ranks
+                                     whatever the size (chunked calls always do) */
+    ARE_DEBUG_RS_SPLIT = 2048u    /* GEMM+RS on the CTA-pair kernel: every unit of a tile reduces its row slice
+                                     (two-shot) whatever the size; not with chunking */
 };
 
 /* Device status word, see are_get_device_status(). */
@@ -181,7 +185,9 @@ typedef struct are_launch_info {
     int32_t block;        /* threads per CTA */
     int32_t cluster;      /* CTAs per cluster (1 or 2) */
     int32_t rank_block;   /* GEMM pair kernel: tile pairs per rank block, 0 = a pair's R units consecutive */
-    int32_t variant;      /* AR kernels: 8-element packs per thread of a row (template variant) */
+    int32_t variant;      /* AR kernels: 8-element packs per thread of a row (template variant); GEMM pair
+                             kernel: 1 = every unit reduces its row slice of the tile (two-shot), 0 = the
+                             GEMM+RS running sum pushed along the ranks */
     int32_t rank_group;   /* GEMM pair kernel: ranks run together inside a rank block (R = ranks innermost) */
     int32_t group_m;      /* GEMM kernels: tile(-pair) rows per raster group */
 } are_launch_info;
@@ -261,16 +267,20 @@ ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t byte
  * order decides when each destination's data completes.
  *  group_m     : 256-row tile pairs per raster group (tile pairs are taken
  *                column by column inside a group of group_m pair rows);
- *                0 = the library's choice (8 for GEMM+RS, 4 otherwise).
+ *                0 = the library's choice (8 for GEMM+RS on the ring, 4
+ *                otherwise).
  *  block_pairs : > 0: tile pairs are taken in blocks of block_pairs, and a
  *                block's units run in rank groups (below); < 0: the R units of
  *                a tile pair run consecutively; 0 = the library's choice.
- *                GEMM+RS pushes a running sum from rank to rank, so it runs
- *                one block of all tile pairs, rank by rank (a pair's R units
- *                consecutive would make each tile's ranks wait on one another
- *                in turn).  Chunked GEMM+RS (are_workspace_set_chunks) with at
- *                least 6 x (co-resident clusters) tile pairs: blocks of two
- *                waves of pairs in rank groups of 2, else consecutive.
+ *                GEMM+RS on the ring pushes a running sum from rank to rank,
+ *                so it runs one block of all tile pairs, rank by rank (a
+ *                pair's R units consecutive would make each tile's ranks wait
+ *                on one another in turn); chunked GEMM+RS
+ *                (are_workspace_set_chunks), always on the ring, runs rank by
+ *                rank in blocks that finish whole chunks (the rotated order:
+ *                one order chunk of every owner segment; the raster: two
+ *                waves of tile pairs).  GEMM+RS with the reduction split over
+ *                a tile's units (R >= 4, up to three waves of units) and
  *                GEMM+AR: consecutive.
  *  rank_group  : with block_pairs > 0, the number of ranks whose units of a
  *                block run together (1 = rank by rank, R = a pair's R units

@@ -1,7 +1,9 @@
 """Which kernel each call launches (the host-side launch record), for the
-workload shapes and the dispatch boundaries: CTA pairs wherever there are at
-least two 128-row tiles and more pair units than co-resident clusters, one
-CTA per tile otherwise; the one-shot AR+RMSNorm kernel up to the per-rank
+workload shapes and the dispatch boundaries: for GEMM+RS CTA pairs wherever
+there are at least two 128-row tiles, with the row-slice split for R >= 4 up
+to three waves of pair units and the ring otherwise; for GEMM+AR CTA pairs
+from one wave of pair units on (also with a single tile row), one CTA per tile
+otherwise; the one-shot AR+RMSNorm kernel up to the per-rank
 byte threshold, the Lamport kernel above it; memsets for an empty
 contraction.  The results themselves are covered by the parity tests."""
 import pytest
@@ -26,20 +28,27 @@ def _gemm(op, R, M, N, K, flags=0):
         return ws.last_launch()
 
 
-@pytest.mark.parametrize("op,R,M,N,K,kernel", [
-    ("rs", 2, 64, 256, 128, "gemm_reduce_kernel"),      # tiny: one tile row
-    ("rs", 4, 256, 4096, 2048, "gemm_reduce_kernel"),   # below one wave of pairs
-    ("rs", 4, 8192, 4096, 2048, "gemm_pair_kernel"),
-    ("rs", 8, 8192, 8192, 4096, "gemm_pair_kernel"),
-    ("ar", 8, 64, 7168, 2048, "gemm_pair_kernel"),     # one tile row: the pair's second tile is empty
-    ("ar", 8, 1, 1000, 128, "gemm_reduce_kernel"),     # below one wave of pairs
-    ("ar", 8, 4096, 7168, 2048, "gemm_pair_kernel"),
-    ("rs", 2, 64, 256, 0, "memset"),
+@pytest.mark.parametrize("op,R,M,N,K,kernel,split", [
+    ("rs", 2, 64, 256, 128, "gemm_reduce_kernel", 0),      # tiny: one tile row
+    ("rs", 4, 256, 4096, 2048, "gemm_pair_kernel", 1),     # below one wave of pairs
+    ("rs", 4, 512, 4096, 2048, "gemm_pair_kernel", 1),     # 1.7 waves
+    ("rs", 2, 256, 4096, 2048, "gemm_pair_kernel", 0),     # a ring of two
+    ("rs", 4, 1024, 4096, 2048, "gemm_pair_kernel", 0),    # 3.4 waves
+    ("rs", 4, 8192, 4096, 2048, "gemm_pair_kernel", 0),
+    ("rs", 8, 8192, 8192, 4096, "gemm_pair_kernel", 0),
+    ("ar", 8, 64, 7168, 2048, "gemm_pair_kernel", 1),     # one tile row: the pair's second tile is empty
+    ("ar", 8, 1, 1000, 128, "gemm_reduce_kernel", 0),     # below one wave of pairs
+    ("ar", 8, 4096, 7168, 2048, "gemm_pair_kernel", 1),
+    ("rs", 2, 64, 256, 0, "memset", 0),
 ])
-def test_gemm_dispatch(op, R, M, N, K, kernel):
+def test_gemm_dispatch(op, R, M, N, K, kernel, split):
+    """The thresholds are stated for the GB300s (76 co-resident clusters
+    of two)."""
     need_gpu()
     li = _gemm(op, R, M, N, K)
     assert li["kernel"] == kernel, li
+    if kernel == "gemm_pair_kernel":
+        assert li["variant"] == split, li
     if kernel == "gemm_pair_kernel":
         assert li["cluster"] == 2 and li["grid"] % 2 == 0 and li["block"] == 384, li
     if kernel == "gemm_reduce_kernel":
@@ -49,8 +58,13 @@ def test_gemm_dispatch(op, R, M, N, K, kernel):
 def test_gemm_debug_flags_force_kernels():
     need_gpu()
     import all_reduce_epilogue_gb300 as are
-    assert _gemm("rs", 4, 256, 4096, 2048, are.DEBUG_PAIR_CTA)["kernel"] == "gemm_pair_kernel"
+    assert _gemm("rs", 4, 256, 4096, 2048, are.DEBUG_SINGLE_CTA)["kernel"] == "gemm_reduce_kernel"
     assert _gemm("rs", 4, 8192, 4096, 2048, are.DEBUG_SINGLE_CTA)["kernel"] == "gemm_reduce_kernel"
+    assert _gemm("ar", 2, 256, 512, 128, are.DEBUG_PAIR_CTA)["kernel"] == "gemm_pair_kernel"
+    li = _gemm("rs", 4, 256, 4096, 2048, are.DEBUG_RS_RING)
+    assert li["kernel"] == "gemm_pair_kernel" and li["variant"] == 0, li
+    li = _gemm("rs", 4, 8192, 4096, 2048, are.DEBUG_RS_SPLIT)
+    assert li["kernel"] == "gemm_pair_kernel" and li["variant"] == 1, li
 
 
 @pytest.mark.parametrize("M,kernel", [(1, "ar_oneshot_kernel"), (16, "ar_oneshot_kernel"),

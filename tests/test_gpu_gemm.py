@@ -126,16 +126,19 @@ def test_segments_equal_contiguous(oracle):
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("kernel", ["default", "pair"])
+@pytest.mark.parametrize("kernel", ["default", "pair", "pair_split"])
 def test_masks_and_owner_pieces_bit_exact(oracle, kernel):
     """With re-arm off, every tile's ready word is (1 << R) - 1 (and words past
     the last tile are 0); each reducer's stored owner pieces equal the
     oracle's cut of the tile at owner boundaries.  After a normal call every
     word is 0 again.  Through the default kernel choice and with the CTA-pair
-    kernel forced wherever it applies."""
+    kernel forced wherever it applies, with either of its GEMM+RS reductions
+    (the ring's last rank, or the last of a tile's R row-slice reducers, logs
+    the tile's pieces and re-arms its word)."""
     need_gpu()
     import all_reduce_epilogue_gb300 as are
-    extra = are.DEBUG_PAIR_CTA if kernel == "pair" else 0
+    extra = {"default": 0, "pair": are.DEBUG_PAIR_CTA | are.DEBUG_RS_RING,
+             "pair_split": are.DEBUG_PAIR_CTA | are.DEBUG_RS_SPLIT}[kernel]
     for (R, M, N, K) in [(2, 64, 256, 128), (4, 256, 1024, 128), (3, 264, 320, 64), (8, 1024, 512, 64)]:
         A, B = synth.gemm_inputs(R, M, N, K, 5)
         with make_ws(debug_flags=are.DEBUG_NO_REARM | are.DEBUG_LOG_PIECES | extra) as ws:
@@ -158,17 +161,20 @@ def test_masks_and_owner_pieces_bit_exact(oracle, kernel):
             assert np.all(ws.snapshot(are.SNAP_MASKS, T * 4).view(np.uint32) == 0)
 
 
-@pytest.mark.parametrize("single_cta", [True, False])
-def test_unpublished_tile_times_out_and_reset_recovers(oracle, single_cta):
+@pytest.mark.parametrize("kernel", ["single", "pair", "pair_split"])
+def test_unpublished_tile_times_out_and_reset_recovers(oracle, kernel):
     """A producer that never sets its ready bit makes the tile's reducer time
     out: the status names the tile, every CTA returns, and a reset recovers.
     Unit 0 is the first producer of tile 0 for the one-CTA kernel, and of the
-    first tile pair (tiles 0 and N/256) for the CTA-pair kernel."""
+    first tile pair (tiles 0 and N/256) for the CTA-pair kernel, where with the
+    row-slice split every unit of that pair waits for it."""
     need_gpu()
     import all_reduce_epilogue_gb300 as are
     R, M, N, K = 4, 256, 512, 128
     A, B = synth.gemm_inputs(R, M, N, K, 8)
-    base = are.DEBUG_SINGLE_CTA if single_cta else are.DEBUG_PAIR_CTA
+    single_cta = kernel == "single"
+    base = {"single": are.DEBUG_SINGLE_CTA, "pair": are.DEBUG_PAIR_CTA | are.DEBUG_RS_RING,
+            "pair_split": are.DEBUG_PAIR_CTA | are.DEBUG_RS_SPLIT}[kernel]
     with make_ws(timeout_ns=20_000_000) as ws:
         ws.set_debug(base | are.DEBUG_SKIP_PUBLISH, 0)
         import torch
@@ -200,14 +206,14 @@ def test_ring_rank_unpublished_mid_chain_times_out(oracle):
     dA, dB = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
     out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with make_ws(timeout_ns=20_000_000) as ws:
-        ws.set_debug(are.DEBUG_PAIR_CTA | are.DEBUG_SKIP_PUBLISH, 4)
+        ws.set_debug(are.DEBUG_PAIR_CTA | are.DEBUG_RS_RING | are.DEBUG_SKIP_PUBLISH, 4)
         are.gemm_rs(dA, dB, out, ws)
         st = ws.device_status()
-        assert ws.last_launch()["kernel"] == "gemm_pair_kernel"
+        assert ws.last_launch()["kernel"] == "gemm_pair_kernel" and ws.last_launch()["variant"] == 0
         assert st["status"] == are.ETIMEOUT and st["code"] in (are.DEV_MASK_TIMEOUT, are.DEV_PIPE_TIMEOUT), st
         if st["code"] == are.DEV_MASK_TIMEOUT:
             assert st["a"] in (0, N // 256), st
-        ws.set_debug(are.DEBUG_PAIR_CTA)
+        ws.set_debug(are.DEBUG_PAIR_CTA | are.DEBUG_RS_RING)
         ws.reset()
         got = host_f32(run_rs(ws, A, B))
     check_close(got, oracle.gemm_rs(A, B), "after reset")
@@ -328,7 +334,8 @@ def test_pair_kernel_matches_single_cta_kernel(mode, R, M, N, K):
     """The CTA-pair kernel (256-row tiles, cta_group::2) and the one-CTA kernel
     compute each output element with the same operations in the same order,
     so their outputs are bitwise identical (several waves, an odd number of
-    tile rows where one CTA of the last pair has no tile)."""
+    tile rows where one CTA of the last pair has no tile); for GEMM+RS so are
+    the pair kernel's two reductions, the ring and the row-slice split."""
     need_gpu()
     import torch
 
@@ -337,7 +344,10 @@ def test_pair_kernel_matches_single_cta_kernel(mode, R, M, N, K):
     dA = [dev_bf16(a) for a in A]
     dB = [dev_bf16(b) for b in B]
     outs = []
-    for flags in (are.DEBUG_PAIR_CTA, are.DEBUG_SINGLE_CTA):
+    kinds = (are.DEBUG_PAIR_CTA, are.DEBUG_SINGLE_CTA)
+    if mode == "rs":
+        kinds += (are.DEBUG_PAIR_CTA | are.DEBUG_RS_RING, are.DEBUG_PAIR_CTA | are.DEBUG_RS_SPLIT)
+    for flags in kinds:
         with make_ws(M_max=M, N_max=N, K_max=K, debug_flags=flags) as ws:
             out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
             if mode == "rs":
@@ -346,7 +356,8 @@ def test_pair_kernel_matches_single_cta_kernel(mode, R, M, N, K):
                 are.gemm_ar(dA, dB, [out] * R, ws)
             assert ws.device_status()["code"] == 0
             outs.append(host_bits(out))
-    assert np.array_equal(outs[0], outs[1])
+    for o in outs[1:]:
+        assert np.array_equal(outs[0], o)
 
 
 @pytest.mark.gpu

@@ -4,7 +4,8 @@ work units run, never the arithmetic: every order must give the same output
 bytes, in both modes, with odd numbers of tile rows (a pair whose second tile
 does not exist) and ragged N; every tile mask is re-armed to 0 after each
 call.  GEMM+AR splits each tile's reduction into R row slices, one per unit of
-the pair (two-shot), which also must not change a byte."""
+the pair (two-shot), which also must not change a byte; GEMM+RS runs every
+order with each of its two reductions, the ring and the row-slice split."""
 import numpy as np
 import pytest
 
@@ -25,7 +26,7 @@ ORDERS = [
 ]
 
 
-@pytest.mark.parametrize("mode", ["rs", "ar"])
+@pytest.mark.parametrize("mode", ["rs", "rs_split", "ar"])
 @pytest.mark.parametrize("R,M,N,K", [(4, 1152, 1000, 192), (3, 768, 520, 64), (8, 2048, 768, 128),
                                      (5, 1280, 256, 128)])
 def test_order_changes_no_output_byte(oracle, mode, R, M, N, K):
@@ -35,15 +36,16 @@ def test_order_changes_no_output_byte(oracle, mode, R, M, N, K):
     import all_reduce_epilogue_gb300 as are
     A, B = synth.gemm_inputs(R, M, N, K, 500 + M + R)
     Ad, Bd = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
-    call = are.gemm_rs if mode == "rs" else are.gemm_ar
+    call = are.gemm_ar if mode == "ar" else are.gemm_rs
+    reduction = {"rs": are.DEBUG_RS_RING, "rs_split": are.DEBUG_RS_SPLIT, "ar": 0}[mode]
     ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with are.Workspace(R_max=8, M_max=M, N_max=N, K_max=K) as ws:
         ws.set_debug(are.DEBUG_SINGLE_CTA)       # the one-CTA kernel: whole-tile reduction
         call(Ad, Bd, ref, ws)
         assert ws.device_status()["code"] == 0
-        Y = oracle.gemm_rs(A, B) if mode == "rs" else oracle.gemm_ar(A, B)
+        Y = oracle.gemm_ar(A, B) if mode == "ar" else oracle.gemm_rs(A, B)
         check_close(host_f32(ref), Y, f"gemm_{mode} one-CTA kernel")
-        ws.set_debug(are.DEBUG_PAIR_CTA)
+        ws.set_debug(are.DEBUG_PAIR_CTA | reduction)
         T = -(-M // 128) * -(-N // 256)
         for order in ORDERS:
             ws.set_gemm_order(*order)

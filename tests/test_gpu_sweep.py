@@ -1,7 +1,7 @@
 """Seeded random shapes for GEMM+RS and GEMM+AR: every rank count of the
 workloads, ragged M and N, several K.  For each shape the CTA-pair kernel (or
-the one-CTA kernel when there is a single tile row) must return the one-CTA
-kernel's bytes, no wait may expire, and the result must match the oracle
+the one-CTA kernel when there is a single tile row; for GEMM+RS both of its reductions,
+the ring and the row-slice split) must return the one-CTA kernel's bytes, no wait may expire, and the result must match the oracle
 within the parity tolerance."""
 import numpy as np
 import pytest
@@ -49,6 +49,16 @@ def test_random_shapes_pair_equals_one_cta_and_oracle(oracle, case):
         call(Ad, Bd, out, ws)
         st = ws.device_status()
         assert st["code"] == 0, st
-    assert np.array_equal(host_bits(out), host_bits(ref)), (mode, R, M, N, K)
+        assert np.array_equal(host_bits(out), host_bits(ref)), (mode, R, M, N, K)
+        if mode == "rs" and M > 128:
+            # both GEMM+RS reductions of the pair kernel: the ring and the row-slice split
+            for flag in (are.DEBUG_RS_RING, are.DEBUG_RS_SPLIT):
+                out.zero_()
+                ws.set_debug(are.DEBUG_PAIR_CTA | flag)
+                call(Ad, Bd, out, ws)
+                st = ws.device_status()
+                assert st["code"] == 0, (flag, st)
+                assert ws.last_launch()["variant"] == (1 if flag == are.DEBUG_RS_SPLIT else 0)
+                assert np.array_equal(host_bits(out), host_bits(ref)), (flag, mode, R, M, N, K)
     Y = oracle.gemm_ar(A, B) if mode == "ar" else oracle.gemm_rs(A, B)
     check_close(host_f32(out), Y, f"{mode} R={R} M={M} N={N} K={K}")
