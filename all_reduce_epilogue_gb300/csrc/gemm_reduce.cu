@@ -1235,21 +1235,31 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                     }
                     // the 128-byte row chunk becomes partial sub-tiles 2j and 2j+1: swizzled smem
                     // staging -> one 8 KB bulk store each; staging buffer b belongs to lane b,
-                    // which waits only for its own bulk group before refilling it
+                    // which waits only for its own bulk group before refilling it.  GEMM+RS with the
+                    // row-slice split alternates two pairs of buffers (the own-slice buffers are GEMM+AR's
+                    // and the slice reduce stages only sOut's first half), so the stores of chunk j - 1
+                    // still read their staging while chunk j is staged (R=4, N=4096, K=2048: M=256
+                    // 33.5-34.2 -> 33.0-33.1 us, M=512 45.8-46.5 -> 45.0-45.7 us; R=8 unchanged)
                     if (own_slice && row >= olo && row < ohi) {
                         // the own slice's rows of sub-tiles 2j, 2j+1, laid out as a loaded stage
                         write_half_sw64<0>(own_buf + (2 * j) * 1024 - olo * 64, row, w);
                         write_half_sw64<1>(own_buf + (2 * j + 1) * 1024 - olo * 64, row, w);
                     }
-                    if (warp == 4 && lane < 2) ptx::bulk_wait_read0();
+                    const bool alt = (MODE == kModeRS) && split && (j & 1);
+                    uint8_t* const stg0 = alt ? sOwn0 : sDrain;
+                    uint8_t* const stg1 = alt ? sOwn1 : sDrain + kPSub2;
+                    if (warp == 4 && lane < 2) {
+                        if ((MODE == kModeRS) && split) ptx::bulk_wait_read1();
+                        else ptx::bulk_wait_read0();
+                    }
                     grp_bar<1>();
-                    write_half_sw64<0>(sDrain, row, w);
-                    write_half_sw64<1>(sDrain + kPSub2, row, w);
+                    write_half_sw64<0>(stg0, row, w);
+                    write_half_sw64<1>(stg1, row, w);
                     ptx::fence_proxy_async_shared();
                     grp_bar<1>();
                     if (warp == 4 && lane < 2) {
                         uint8_t* dst = gdst + (size_t)(2 * j + lane) * kPSub2;
-                        const uint8_t* src = sDrain + lane * kPSub2;
+                        const uint8_t* src = lane ? stg1 : stg0;
                         if (own_slice) {  // every row but the own slice's
                             if (olo > 0) ptx::bulk_store(dst, src, (uint32_t)(olo * 64));
                             if (ohi < kBM) ptx::bulk_store(dst + ohi * 64, src + ohi * 64, (uint32_t)((kBM - ohi) * 64));
