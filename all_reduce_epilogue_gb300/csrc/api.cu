@@ -271,6 +271,11 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
         p->chunks = ws->chunks;
     }
     if (use_pair) {
+        // the partial slots as a 5-D map: a row slice's 16-row group of 8 sub-tiles in one load
+        if (make_tmap_part(&p->tmPart, ws->d_part, (uint64_t)T, (uint64_t)R) != cudaSuccess) {
+            delete p;
+            return ARE_EINVAL;
+        }
         p->group_m = (int)std::min<int64_t>(p->pairs_m, 4);
         const int64_t num_pairs = (int64_t)p->pairs_m * tiles_n;
         // destination-rotated order (chunked GEMM+RS): needs owner segments of whole pair

@@ -99,6 +99,9 @@ struct GemmParams {
     CUtensorMap tmB[kMaxRanks];
     CUtensorMap tmOut[kMaxRanks];  // GEMM+RS: owner segments (64 x H boxes); GEMM+AR: the distinct views
                                    // (64 x 128 boxes for the one-CTA kernel, 64 x 16 for the pair kernel)
+    // CTA-pair kernel: the partial slots as [R][T][16 sub-tiles][128 rows][16 words], boxes of
+    // 8 sub-tiles x 16 rows (one 8 KB partial-buffer stage of a row slice's 16-row group)
+    CUtensorMap tmPart;
     are_bf16* views[kMaxRanks];  // GEMM+AR: distinct output views; GEMM+RS with rs_split: the owner
                                  // segments (row groups that no box covers: st.global)
     uint8_t* part;       // [R][T][tile part bytes]
@@ -138,6 +141,8 @@ cudaError_t gemm_prepare_kernels();
 // bf16 [outer, inner] row-major tensor map, 128B-swizzled boxes of box_inner x box_outer.
 cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                            uint32_t box_outer);
+// The pair kernel's partial slots for T tiles and R ranks as a 5-D map (see GemmParams::tmPart).
+cudaError_t make_tmap_part(CUtensorMap* m, const void* part, uint64_t T, uint64_t R);
 cudaError_t launch_gemm_reduce(const GemmParams& p, int mode, int grid, cudaStream_t stream);
 // CTA-pair variant (cta_group::2 UMMA, 256x256 per pair); grid = 2 x clusters.
 cudaError_t launch_gemm_pair(const GemmParams& p, int mode, int grid, cudaStream_t stream);

@@ -1096,20 +1096,18 @@ __global__ void __launch_bounds__(kPairThreads, 1) gemm_pair_kernel(const __grid
                 ptx::fence_proxy_async_global();
                 // row slice U.j: groups of up to 16 rows; a stage holds one rank's group of 8
                 // sub-tiles, 1 KB per 64-byte column sub-tile (sub-tile hf * 8 + st at st * 1 KB of
-                // the group's stage hf); each slice of a partial is read once, so evict-first
+                // the group's stage hf), fetched by one 5-D tile load (rows past the tile's 128 read
+                // as zeros, rows past the slice are not used); each slice of a partial is read once,
+                // so evict-first
                 const int lo = U.j * kBM / p.R, hi = (U.j + 1) * kBM / p.R;
                 const uint64_t pol_p = ptx::policy_evict_first();
                 for (int g0 = lo; g0 < hi && ok; g0 += 16) {
-                    const int nr = min(16, hi - g0);
                     for (int hf = 0; hf < kHalves && ok; ++hf) {
                         for (int r = 0; r < p.R; ++r) {
                             if (own_slice && r == U.j) continue;  // on chip (sOwn)
                             if (!wait_bar(&pempty[ps], pph ^ 1u, abort_flag, p, 13, u)) { ok = false; break; }
-                            ptx::mbar_arrive_expect_tx(&pfull[ps], (uint32_t)(8 * nr * 64));
-                            const uint8_t* src = pair_slot(p, U, r) + (size_t)(hf * 8) * kPSub2 + (size_t)g0 * 64;
-                            for (int st = 0; st < 8; ++st)
-                                ptx::bulk_load_hint(sP + ps * kPSub2 + st * 1024, src + (size_t)st * kPSub2,
-                                                    (uint32_t)(nr * 64), &pfull[ps], pol_p);
+                            ptx::mbar_arrive_expect_tx(&pfull[ps], kPSub2);
+                            ptx::tma_load_5d(sP + ps * kPSub2, &p.tmPart, &pfull[ps], 0, g0, hf * 8, U.t, r, pol_p);
                             issued |= 1u << ps;
                             issued_ph = (issued_ph & ~(1u << ps)) | (pph << ps);
                             if (++ps == kPStages2) { ps = 0; pph ^= 1u; }
@@ -1629,6 +1627,20 @@ cudaError_t make_tmap_bf16(CUtensorMap* m, const void* base, uint64_t inner, uin
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_part(CUtensorMap* m, const void* part, uint64_t T, uint64_t R) {
+    cudaError_t e = get_encode();
+    if (e != cudaSuccess) return e;
+    // 4-byte words: 16 per 64-byte sub-tile row, 128 rows, 16 sub-tiles per 128 KB slot
+    cuuint64_t dims[5] = {16, 128, 16, T, R};
+    cuuint64_t strides[4] = {64, (cuuint64_t)kPSub2, (cuuint64_t)kTilePartBytes, (cuuint64_t)T * kTilePartBytes};
+    cuuint32_t box[5] = {16, 16, 8, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 5, const_cast<void*>(part), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
