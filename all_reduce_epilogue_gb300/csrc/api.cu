@@ -211,10 +211,10 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     // reducing its row slice (two-shot, as GEMM+AR).  The ring's R drains of a tile run one after
     // the other, which a problem of many waves hides and one of a few waves does not.  Measured
     // (us per call, ring / split / one-CTA kernel; waves of pair units): R=4, N=4096, K=2048 at
-    // M=256 42.7 / 33.6 / 35.4 (0.8), M=512 52.4 / 46.1 / 54.1 (1.7), M=1024 62.1 / 68.1 / 89.9
-    // (3.4), M=4096 172.7 / 199.0 / 239.1; R=8, N=7168, K=2048, M=256 97.5 / 75.4 / 118.4 (2.9);
-    // R=8, N=8192, K=4096, M=512 174.7 / 198.2 / 268.4 (6.7); R=2, N=4096, K=2048, M=256
-    // 26.3 / 30.0 / 29.1 (0.4: a chain of two).  So: the split for R >= 4 up to three waves, the
+    // M=256 44.1 / 29.9 / 35.2 (0.8), M=512 52.6 / 41.2 / 53.3 (1.7), M=1024 61.7 / 63.8 / 88.6
+    // (3.4), M=4096 173.1 / 194.7 / 235.9; R=8, N=7168, K=2048, M=256 98.7 / 68.9 / 118.1 (2.9);
+    // R=8, N=8192, K=4096, M=512 176.9 / 196.4 / 269.7 (6.7); R=2, N=4096, K=2048, M=256
+    // 26.9 / 27.0 / 29.0 (0.4: a chain of two).  So: the split for R >= 4 up to three waves, the
     // ring otherwise, and the pair kernel (either way) rather than the one-CTA kernel from two
     // tile rows on.  Chunked calls count a tile's pieces at the ring's last rank: always the ring.
     bool rs_split = mode == kModeRS && ws->chunks == 0 && R >= 4 && pair_units <= 3 * (int64_t)clusters;
