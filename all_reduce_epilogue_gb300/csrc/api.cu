@@ -206,7 +206,6 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     // SM streaming (R=8, M=64, N=7168, K=2048: 58.6 against 64.5 us).
     const int clusters = ws->pair_clusters;
     const int64_t pair_units = (int64_t)((tiles_m + 1) / 2) * tiles_n * R;
-    const bool pair_ok = (tiles_m >= 2 || mode == kModeAR) && clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
     // GEMM+RS on the pair kernel: the running sum pushed along the ranks, or every unit of a tile
     // reducing its row slice (two-shot, as GEMM+AR).  The ring's R drains of a tile run one after
     // the other, which a problem of many waves hides and one of a few waves does not.  Measured
@@ -220,6 +219,13 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     bool rs_split = mode == kModeRS && ws->chunks == 0 && R >= 4 && pair_units <= 3 * (int64_t)clusters;
     if (ws->debug_flags & ARE_DEBUG_RS_SPLIT) rs_split = mode == kModeRS && ws->chunks == 0;
     if (ws->debug_flags & ARE_DEBUG_RS_RING) rs_split = false;
+    // A single tile row (the pair's second tile does not exist, as with any odd number of tile
+    // rows) takes the pair kernel for GEMM+AR and for the GEMM+RS split: R=4, M=128, N=4096,
+    // K=2048 29.1 against 35.8-36.1 us here and 44.9 on the ring, R=8, M=128, N=7168 62.5 against
+    // 90.7 and 96.0; with R < 4 the one-CTA kernel stays ahead (R=2, M=64, N=256, K=128 14.1-14.3
+    // against 16.6-17.0 us, R=2, M=128, N=1024, K=512 16.8-17.1 against 18.5-19.2).
+    const bool pair_ok = (tiles_m >= 2 || mode == kModeAR || rs_split || (ws->debug_flags & ARE_DEBUG_PAIR_CTA)) &&
+                         clusters > 0 && !(ws->debug_flags & ARE_DEBUG_SINGLE_CTA);
     // GEMM+AR below one wave of pairs: the one-CTA kernel (the pair kernel from one wave on, or
     // with a single tile row, see above)
     const bool use_pair = pair_ok && (pair_units > clusters || mode == kModeRS || (ws->debug_flags & ARE_DEBUG_PAIR_CTA));

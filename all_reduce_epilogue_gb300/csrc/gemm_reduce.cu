@@ -19,10 +19,13 @@
 // piece is stored into its owner's segment.
 //
 // One-GPU design.  Two kernels implement it.  gemm_pair_kernel (further down)
-// runs a CTA pair per 256x256 block with cta_group::2 MMAs and is used
-// whenever there are at least two 128-row tiles; gemm_reduce_kernel (next),
-// one CTA per 128x256 tile, covers the rest.  Both share the workspace layout,
-// the mask protocol and the owner-piece stores.
+// runs a CTA pair per 256x256 block with cta_group::2 MMAs; it takes GEMM+RS
+// from two 128-row tiles on and GEMM+AR from one wave of tile pairs on (the
+// host's dispatch also picks its GEMM+RS reduction: the running sum pushed
+// along the ranks, or the row slices split over a tile's units for problems
+// of a few waves).  gemm_reduce_kernel (next), one CTA per 128x256 tile,
+// covers the rest.  Both share the workspace layout, the mask protocol and the
+// owner-piece stores, and give the same bytes.
 //
 // gemm_reduce_kernel.  A work unit is (rank r, output tile t), a 128x256 tile of
 // P_r = A_r B_r with K = K_r.  Units are ordered tile-major with the tile's

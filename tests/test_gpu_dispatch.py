@@ -1,7 +1,8 @@
 """Which kernel each call launches (the host-side launch record), for the
 workload shapes and the dispatch boundaries: for GEMM+RS CTA pairs wherever
 there are at least two 128-row tiles, with the row-slice split for R >= 4 up
-to three waves of pair units and the ring otherwise; for GEMM+AR CTA pairs
+to three waves of pair units (then also with a single tile row) and the ring
+otherwise; for GEMM+AR CTA pairs
 from one wave of pair units on (also with a single tile row), one CTA per tile
 otherwise; the one-shot AR+RMSNorm kernel up to the per-rank
 byte threshold, the Lamport kernel above it; memsets for an empty
@@ -29,7 +30,9 @@ def _gemm(op, R, M, N, K, flags=0):
 
 
 @pytest.mark.parametrize("op,R,M,N,K,kernel,split", [
-    ("rs", 2, 64, 256, 128, "gemm_reduce_kernel", 0),      # tiny: one tile row
+    ("rs", 2, 64, 256, 128, "gemm_reduce_kernel", 0),      # tiny: one tile row, R < 4
+    ("rs", 4, 128, 4096, 2048, "gemm_pair_kernel", 1),     # one tile row, the split (the pair's second tile absent)
+    ("rs", 8, 128, 7168, 2048, "gemm_pair_kernel", 1),
     ("rs", 4, 256, 4096, 2048, "gemm_pair_kernel", 1),     # below one wave of pairs
     ("rs", 4, 512, 4096, 2048, "gemm_pair_kernel", 1),     # 1.7 waves
     ("rs", 2, 256, 4096, 2048, "gemm_pair_kernel", 0),     # a ring of two
