@@ -67,10 +67,13 @@ def test_allreduce_rmsnorm_graph_replays(oracle, path, M):
         assert np.all(words == SENT)
 
 
-def test_gemm_rs_and_ar_graph_replays(oracle):
+@pytest.mark.parametrize("reduction", ["default", "ring"])
+def test_gemm_rs_and_ar_graph_replays(oracle, reduction):
     """GEMM+RS and GEMM+AR captured together and replayed: the tile masks are
-    re-armed by the reducers, so every replay waits for that replay's own
-    partials."""
+    re-armed by the reducers (the ring's last rank, or the last of a tile's
+    row-slice reducers, whose per-tile count also returns to 0), so every
+    replay waits for that replay's own partials.  At this size GEMM+RS takes
+    the row-slice split by default; the ring is forced in the second case."""
     need_gpu()
     import torch
 
@@ -81,6 +84,8 @@ def test_gemm_rs_and_ar_graph_replays(oracle):
     out_rs = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     out_ar = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with are.Workspace(R_max=8, M_max=M, N_max=N, K_max=K, timeout_ns=100_000_000) as ws:
+        if reduction == "ring":
+            ws.set_debug(are.DEBUG_RS_RING)
         for t in dA + dB:
             t.zero_()
 
