@@ -124,8 +124,8 @@ enum {
                                      to the counters (see ARE_SNAP_COUNTERS) */
     ARE_DEBUG_AR_ONESHOT = 128u,  /* AR+RMSNorm: take the one-shot path whatever the size (where a row fits) */
     ARE_DEBUG_AR_LAMPORT = 256u,  /* AR+RMSNorm: take the Lamport path whatever the size */
-    ARE_DEBUG_PAIR_CTA = 512u,    /* GEMM: use the CTA-pair kernel wherever it applies (two or more tile rows;
-                                     GEMM+AR also one), also below one wave of pairs */
+    ARE_DEBUG_PAIR_CTA = 512u,    /* GEMM: use the CTA-pair kernel whatever the size (also with a single tile
+                                     row, where the pair's second tile is absent, and below one wave) */
     ARE_DEBUG_RS_RING = 1024u,    /* GEMM+RS on the CTA-pair kernel: push the running sum along the ranks
                                      whatever the size (chunked calls always do) */
     ARE_DEBUG_RS_SPLIT = 2048u    /* GEMM+RS on the CTA-pair kernel: every unit of a tile reduces its row slice
