@@ -97,6 +97,33 @@ def test_gemm_rs_r4_sampled(oracle, M):
     check_close(got, oracle.gemm_rs(A, B, rows), f"gemm_rs R=4 M={M} sampled")
 
 
+@pytest.mark.parametrize("R,N", [(4, 4096), (8, 7168)])
+def test_gemm_rs_single_tile_row_split(oracle, R, N):
+    """GEMM+RS with a single 128-row tile at R >= 4 takes the CTA-pair kernel's
+    row-slice split by default (the pair's second tile is absent): the launch
+    record says so, the bytes equal the one-CTA kernel's, and the full result
+    matches the oracle.  M=128, K=2048, owner segments of 128/R rows."""
+    need_gpu()
+    import torch
+
+    import all_reduce_epilogue_gb300 as are
+    M, K = 128, 2048
+    A, B = synth.gemm_inputs(R, M, N, K, 4100 + R)
+    dA, dB = [dev_bf16(a) for a in A], [dev_bf16(b) for b in B]
+    with make_ws(M_max=M, N_max=N, K_max=K) as ws:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        are.gemm_rs(dA, dB, out, ws)
+        assert ws.device_status()["code"] == 0
+        li = ws.last_launch()
+        assert li["kernel"] == "gemm_pair_kernel" and li["variant"] == 1, li
+        ref = torch.empty_like(out)
+        ws.set_debug(are.DEBUG_SINGLE_CTA)
+        are.gemm_rs(dA, dB, ref, ws)
+        assert ws.device_status()["code"] == 0
+    assert np.array_equal(host_bits(out), host_bits(ref))
+    check_close(host_f32(out), oracle.gemm_rs(A, B), f"gemm_rs R={R} M={M} N={N} single tile row")
+
+
 def test_integer_inputs_bit_exact(oracle):
     """Small integer operands: every partial and sum is exact in fp32, so the
     bf16 output must equal the oracle's rounding bit for bit."""
