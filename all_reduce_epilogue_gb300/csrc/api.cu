@@ -313,6 +313,14 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
                 // tile's drains then wait in a chain).
                 p->block_tiles = (int)num_pairs;
                 p->group_m = (int)std::min<int64_t>(p->pairs_m, 8);
+                // With most of a wave of pairs but not a whole one, a tile's consecutive ranks would
+                // share waves and its drains wait in a chain; a block padded to one wave runs each
+                // rank in a wave of its own.  That pays where units are short (K <= 2048): R=4,
+                // M=1024, N=4096, K=2048 (64 pairs) 61.7 -> 55.1 us, R=2 the same 38.0 -> 32.1,
+                // R=3, M=768 (48 pairs) 45.6 -> 42.1; not with long units or a sparse wave (R=8,
+                // M=512, N=8192, K=4096, 64 pairs 176.0 -> 186.7; R=2, M=256, 16 pairs 26.7 -> 30.1).
+                if (num_pairs < clusters && 10 * num_pairs >= 6 * (int64_t)clusters && K <= 2048)
+                    p->block_tiles = clusters;
             } else {
                 // chunked GEMM+RS completes chunks early: blocks that finish whole chunks, one
                 // order chunk of every segment each in the destination-rotated order, else two

@@ -58,6 +58,21 @@ def test_gemm_dispatch(op, R, M, N, K, kernel, split):
         assert li["cluster"] == 1 and li["block"] == 256, li
 
 
+def test_ring_block_is_padded_to_a_wave_for_short_units():
+    """GEMM+RS on the ring with most of a wave of tile pairs but not a whole one
+    runs each rank in a wave of its own (a block padded to the co-resident
+    clusters) when its units are short (K <= 2048); otherwise one block of the
+    actual pairs."""
+    need_gpu()
+    li = _gemm("rs", 4, 1024, 4096, 2048)        # 64 tile pairs
+    clusters = li["grid"] // 2
+    assert li["variant"] == 0 and li["rank_block"] == clusters > 64, li
+    li = _gemm("rs", 8, 512, 8192, 4096)         # 64 tile pairs, K = 4096
+    assert li["variant"] == 0 and li["rank_block"] == 64, li
+    li = _gemm("rs", 2, 256, 4096, 2048)         # 16 tile pairs: a sparse wave
+    assert li["variant"] == 0 and li["rank_block"] == 16, li
+
+
 def test_gemm_debug_flags_force_kernels():
     need_gpu()
     import all_reduce_epilogue_gb300 as are
