@@ -208,15 +208,18 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     const int64_t pair_units = (int64_t)((tiles_m + 1) / 2) * tiles_n * R;
     // GEMM+RS on the pair kernel: the running sum pushed along the ranks, or every unit of a tile
     // reducing its row slice (two-shot, as GEMM+AR).  The ring's R drains of a tile run one after
-    // the other, which a problem of many waves hides and one of a few waves does not.  Measured
-    // (us per call, ring / split / one-CTA kernel; waves of pair units): R=4, N=4096, K=2048 at
-    // M=256 44.1 / 29.9 / 35.2 (0.8), M=512 52.6 / 41.2 / 53.3 (1.7), M=1024 61.7 / 63.8 / 88.6
-    // (3.4), M=4096 173.1 / 194.7 / 235.9; R=8, N=7168, K=2048, M=256 98.7 / 68.9 / 118.1 (2.9);
-    // R=8, N=8192, K=4096, M=512 176.9 / 196.4 / 269.7 (6.7); R=2, N=4096, K=2048, M=256
-    // 26.9 / 27.0 / 29.0 (0.4: a chain of two).  So: the split for R >= 4 up to three waves, the
-    // ring otherwise, and the pair kernel (either way) rather than the one-CTA kernel from two
-    // tile rows on.  Chunked calls count a tile's pieces at the ring's last rank: always the ring.
-    bool rs_split = mode == kModeRS && ws->chunks == 0 && R >= 4 && pair_units <= 3 * (int64_t)clusters;
+    // the other, which a wave or more of tile pairs (or a block padded to one, see the unit order)
+    // hides and fewer pairs do not.  Measured (us per call, ring / split / one-CTA kernel; tile
+    // pairs, of 76 co-resident clusters): R=4, N=4096, K=2048 at M=256 44.0 / 29.8 / 35.2 (16),
+    // M=512 52.3 / 41.3 / 52.8 (32), M=768 53.2 / 52.0 (48), M=1024 54.1 (padded) / 62.6 / 88.6
+    // (64), M=4096 171.5 / 192.2 / 235.0 (256); R=8, K=2048, M=256, N=7168 98.9 / 69.7 / 118.0
+    // (28), M=384, N=4096 91.5 / 68.1 (32), M=256, N=8192 103.1 / 82.1 (32); R=8, N=8192,
+    // K=4096, M=512 173.8 / 193.3 / 266.6 (64); R=2, N=4096, K=2048, M=256 26.8 / 27.0 / 29.1 (16:
+    // a chain of two).  So: the split for R >= 4 up to three quarters of a wave of pairs, the ring
+    // otherwise, and the pair kernel (either way) rather than the one-CTA kernel from two tile
+    // rows on.  Chunked calls count a tile's pieces at the ring's last rank: always the ring.
+    const int64_t num_pairs_all = (int64_t)((tiles_m + 1) / 2) * tiles_n;
+    bool rs_split = mode == kModeRS && ws->chunks == 0 && R >= 4 && 4 * num_pairs_all <= 3 * (int64_t)clusters;
     if (ws->debug_flags & ARE_DEBUG_RS_SPLIT) rs_split = mode == kModeRS && ws->chunks == 0;
     if (ws->debug_flags & ARE_DEBUG_RS_RING) rs_split = false;
     // A single tile row (the pair's second tile does not exist, as with any odd number of tile

@@ -275,12 +275,13 @@ ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t byte
  *                GEMM+RS on the ring pushes a running sum from rank to rank,
  *                so it runs one block of all tile pairs, rank by rank (a
  *                pair's R units consecutive would make each tile's ranks wait
- *                on one another in turn); chunked GEMM+RS
+ *                on one another in turn), padded to one wave of pairs where
+ *                the pairs fill 60-100 % of a wave and K <= 2048; chunked GEMM+RS
  *                (are_workspace_set_chunks), always on the ring, runs rank by
  *                rank in blocks that finish whole chunks (the rotated order:
  *                one order chunk of every owner segment; the raster: two
  *                waves of tile pairs).  GEMM+RS with the reduction split over
- *                a tile's units (R >= 4, up to three waves of units) and
+ *                a tile's units (R >= 4, up to 3/4 of a wave of tile pairs) and
  *                GEMM+AR: consecutive.
  *  rank_group  : with block_pairs > 0, the number of ranks whose units of a
  *                block run together (1 = rank by rank, R = a pair's R units
