@@ -219,14 +219,18 @@ are_status gemm_call(int mode, const are_bf16* const A[], const are_bf16* const 
     // 92.9 / 98.3; R=4, M=768 52.3 / 53.2) but not for R=5 and 6 (R=6, M=768 80.5 / 73.9; R=5,
     // M=640 71.6 / 62.4), whose row slices are not whole 16-row groups (more, partly empty stage
     // loads and whole-row stores instead of TMA boxes); at 32 pairs it leads for those too (R=6,
-    // M=384 63.2 / 71.0).  So: the split for R = 4 and 8 up to three quarters of a wave of pairs
-    // and for R = 5..7 up to half a wave, the ring otherwise, and the pair kernel (either way)
-    // rather than the one-CTA kernel from two tile rows on.  Chunked calls count a tile's pieces
-    // at the ring's last rank: always the ring.
+    // M=384 63.2 / 71.0).  Long units hide more of the ring's chain: at K=4096 with 56 pairs the
+    // ring leads (R=8, M=384, N=7168 152.9 / 161.5), with 32 the two tie for R=8 (M=256, N=8192
+    // 132.4 / 131.9) and the split leads for R=4 (M=512 67.7 / 63.2).  So: the split for R = 4
+    // and 8 up to three quarters of a wave of pairs when K <= 2048, and otherwise (R = 5..7, or
+    // longer K) up to half a wave; the ring beyond that; and the pair kernel (either way) rather
+    // than the one-CTA kernel from two tile rows on.  Chunked calls count a tile's pieces at the
+    // ring's last rank: always the ring.
     const int64_t num_pairs_all = (int64_t)((tiles_m + 1) / 2) * tiles_n;
     const bool whole_groups = kBM % (16 * R) == 0;  // R = 4, 8: every row slice is 16-row groups
     bool rs_split = mode == kModeRS && ws->chunks == 0 && R >= 4 &&
-                    (whole_groups ? 4 * num_pairs_all <= 3 * (int64_t)clusters : 2 * num_pairs_all <= (int64_t)clusters);
+                    ((whole_groups && K <= 2048) ? 4 * num_pairs_all <= 3 * (int64_t)clusters
+                                                 : 2 * num_pairs_all <= (int64_t)clusters);
     if (ws->debug_flags & ARE_DEBUG_RS_SPLIT) rs_split = mode == kModeRS && ws->chunks == 0;
     if (ws->debug_flags & ARE_DEBUG_RS_RING) rs_split = false;
     // A single tile row (the pair's second tile does not exist, as with any odd number of tile

@@ -281,8 +281,8 @@ ARE_API are_status are_workspace_set_oneshot_max_bytes(are_ws* ws, uint64_t byte
  *                rank in blocks that finish whole chunks (the rotated order:
  *                one order chunk of every owner segment; the raster: two
  *                waves of tile pairs).  GEMM+RS with the reduction split over
- *                a tile's units (R = 4, 8 up to 3/4 of a wave of tile pairs,
- *                R = 5..7 up to half a wave) and
+ *                a tile's units (R = 4, 8 with K <= 2048 up to 3/4 of a wave of
+ *                tile pairs, otherwise up to half a wave) and
  *                GEMM+AR: consecutive.
  *  rank_group  : with block_pairs > 0, the number of ranks whose units of a
  *                block run together (1 = rank by rank, R = a pair's R units

@@ -1,8 +1,8 @@
 """Which kernel each call launches (the host-side launch record), for the
 workload shapes and the dispatch boundaries: for GEMM+RS CTA pairs wherever
 there are at least two 128-row tiles, with the row-slice split for R = 4 and 8
-up to three quarters of a wave of tile pairs and for R = 5..7 up to half a wave
-(then also with a single tile row), and the ring otherwise; for GEMM+AR CTA pairs
+with K <= 2048 up to three quarters of a wave of tile pairs and otherwise up to
+half a wave (then also with a single tile row), and the ring beyond; for GEMM+AR CTA pairs
 from one wave of pair units on (also with a single tile row), one CTA per tile
 otherwise; the one-shot AR+RMSNorm kernel up to the per-rank
 byte threshold, the Lamport kernel above it; memsets for an empty
@@ -38,6 +38,8 @@ def _gemm(op, R, M, N, K, flags=0):
     ("rs", 8, 384, 4096, 2048, "gemm_pair_kernel", 1),     # 32 tile pairs, 3.4 waves of units
     ("rs", 6, 384, 4096, 2048, "gemm_pair_kernel", 1),     # R = 6: 32 tile pairs, up to half a wave
     ("rs", 6, 768, 4096, 2048, "gemm_pair_kernel", 0),     # R = 6: 48 tile pairs, the ring
+    ("rs", 8, 384, 7168, 2048, "gemm_pair_kernel", 1),     # 56 tile pairs, K = 2048: the split
+    ("rs", 8, 384, 7168, 4096, "gemm_pair_kernel", 0),     # 56 tile pairs, K = 4096: the ring
     ("rs", 2, 256, 4096, 2048, "gemm_pair_kernel", 0),     # a ring of two
     ("rs", 4, 1024, 4096, 2048, "gemm_pair_kernel", 0),    # 64 tile pairs: the ring (a padded block)
     ("rs", 4, 8192, 4096, 2048, "gemm_pair_kernel", 0),
